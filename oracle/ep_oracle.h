@@ -1,0 +1,75 @@
+/*
+ * ep_oracle.h -- plain, single-threaded CPU oracle for MoE expert-parallel
+ * routing layout, dispatch (BF16 and FP8 e4m3 with per-128-channel scales)
+ * and weighted top-k combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this library: only the test-suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header, table or constant
+ * with the CUDA library and includes no CUDA header.
+ *
+ * Every function computes the plain definition of its step; see the comments
+ * in ep_oracle.c for the passage each one follows and the reading taken where
+ * the pages leave a step open.
+ */
+#ifndef EP_ORACLE_H
+#define EP_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_LAYOUT_CONTIGUOUS = 0, ORACLE_LAYOUT_MASKED = 1 };
+enum { ORACLE_FLAG_BAD_EXPERT = 1u, ORACLE_FLAG_OVERFLOW = 2u };
+
+/* Scalar format helpers (definitions of the number formats). */
+float    oracle_bf16_to_float(uint16_t b);
+uint16_t oracle_bf16_from_double(double v);
+float    oracle_e4m3_decode(uint8_t code);
+uint8_t  oracle_e4m3_encode(float v);
+
+/* Routing layout.  topk_idx is [T,k] row-major.  Writes counts[E],
+ * offsets[E+1], dst_row[T*k] and, if rank_token_counts is not NULL,
+ * rank_token_counts[R].  Returns the OR of ORACLE_FLAG_* conditions.
+ * Returns 0xFFFFFFFF (and writes nothing) on invalid sizes. */
+uint32_t oracle_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                       int kind, int capacity, int32_t* counts,
+                       int32_t* offsets, int32_t* dst_row,
+                       int32_t* rank_token_counts);
+
+/* BF16 dispatch: recv[dst_row[t,j], :] = x[t, :] for every pair with
+ * dst_row >= 0.  x is [T,H], recv is [rows,H], both bf16 bit patterns. */
+void oracle_dispatch_bf16(const uint16_t* x, int64_t T, int64_t H, int k,
+                          const int32_t* dst_row, uint16_t* recv);
+
+/* Per-token, per-128-channel FP8 e4m3 quantisation of one token row:
+ * q[H] codes and scale[H/128] float32.  H must be a multiple of 128. */
+void oracle_quantize_row_fp8(const uint16_t* x_row, int64_t H, uint8_t* q,
+                             float* scale);
+
+/* FP8 dispatch: the quantised row and its scales copied to every dst_row of
+ * the token.  recv_q is [rows,H] e4m3 codes, recv_scale is [rows,H/128]. */
+void oracle_dispatch_fp8(const uint16_t* x, int64_t T, int64_t H, int k,
+                         const int32_t* dst_row, uint8_t* recv_q,
+                         float* recv_scale);
+
+/* Combine with fp64 accumulation.  out[t,h] = bf16(sum_j w[t,j]*y[row,h])
+ * rounded once from the fp64 sum.  ref (may be NULL) receives the fp64 sum,
+ * absum (may be NULL) the fp64 sum of |w*y| over the valid pairs. */
+void oracle_combine_f64(const uint16_t* y, const float* topk_w,
+                        const int32_t* dst_row, int64_t T, int64_t H, int k,
+                        uint16_t* out, double* ref, double* absum);
+
+/* Combine as a sequence of fp32 fused multiply-adds in increasing j, each
+ * rounded to nearest even, then rounded once to bf16. */
+void oracle_combine_fp32_seq(const uint16_t* y, const float* topk_w,
+                             const int32_t* dst_row, int64_t T, int64_t H,
+                             int k, uint16_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
