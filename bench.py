@@ -1,0 +1,478 @@
+"""Benchmark: one step = routing layout + dispatch + combine on one batch.
+
+Default workload: the Prefill-like shape (65,536 tokens = 16 virtual ranks x
+4,096, hidden 7168, 256 experts, top-8 with Zipf(1.0) popularity, contiguous
+layout, BF16 dispatch and combine; combine runs over the dispatched rows,
+i.e. identity experts).  Inputs are generated on the device before timing
+and are far larger than L2 (x 0.94 GB, dispatch buffer 7.5 GB), so no L2
+flush is inserted between steps.
+
+Prints ONE JSON line (rank 0).  `value` is the logical throughput: the
+useful payload of one dispatch plus one combine (each (token, expert)
+assignment counted once; BF16 T*k*H*2 each way, FP8 dispatch T*k*(H + H/32))
+divided by the device time of the whole step, summed over all ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+import torch.distributed as dist
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from combine_ep_layout_02_gb300 import workloads as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "dispatch+combine logical GB/s per call (layout+dispatch+combine, one event pair)"
+KERNEL_SOURCES = {
+    "layout": "combine_ep_layout_02_gb300/csrc/ep_layout.cu",
+    "dispatch": "combine_ep_layout_02_gb300/csrc/ep_dispatch.cu",
+    "dispatch_fp8": "combine_ep_layout_02_gb300/csrc/ep_dispatch.cu",
+    "combine": "combine_ep_layout_02_gb300/csrc/ep_combine.cu",
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="prefill", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="scale the workload to this many tokens (profiling captures)")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the timed oracle sample (cpu_baseline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def max_over_ranks(value, world, device=None):
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world, device=None):
+    if world > 1:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate_value(logical_bytes_per_step, steps, max_seconds, world):
+    """Whole-job logical GB/s: every rank processes its own step each time."""
+    return world * logical_bytes_per_step * steps / max_seconds / 1e9
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        for key in ("hbm_gbs", "hbm_copy_gbs", "hbm_GBs"):
+            if key in peaks and peaks[key]:
+                return float(peaks[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            tab = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = tab.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ident = vis.split(",")[device_index] if vis else str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, IndexError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(wl, x_host_bits, idx_host, w_host, tokens, seconds):
+    """Time the CPU oracle (layout + dispatch + combine of `tokens` tokens) in
+    repeated passes until `seconds` elapse; return logical GB/s and details."""
+    import oracle
+    T = tokens
+    idx = idx_host[:T]
+    xb = x_host_bits[:T]
+    w = w_host[:T]
+    kind = oracle.LAYOUT_MASKED if wl.kind == "masked" else oracle.LAYOUT_CONTIGUOUS
+    cap = min(wl.capacity, T) if wl.kind == "masked" else 0
+    rows = T * wl.k if wl.kind == "contiguous" else wl.E * cap
+    disp_b, comb_b = wl.scaled(T=T).logical_bytes()
+    passes, t_lay, t_disp, t_comb = 0, 0.0, 0.0, 0.0
+    t0 = time.perf_counter()
+    while True:
+        a = time.perf_counter()
+        lay = oracle.layout(idx, wl.E, wl.R, kind, cap)
+        b = time.perf_counter()
+        if wl.payload == "fp8":
+            oracle.dispatch_fp8(xb, lay["dst_row"], rows)
+        recv = oracle.dispatch_bf16(xb, lay["dst_row"], rows)
+        c = time.perf_counter()
+        oracle.combine_f64(recv, w, lay["dst_row"])
+        d = time.perf_counter()
+        passes += 1
+        t_lay, t_disp, t_comb = t_lay + b - a, t_disp + c - b, t_comb + d - c
+        if d - t0 >= seconds:
+            break
+    total = t_lay + t_disp + t_comb
+    return {
+        "value": passes * (disp_b + comb_b) / total / 1e9,
+        "unit": "GB/s",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": "%d passes of layout+dispatch+combine over the first %d of %d tokens "
+                  "(%.1f s, single-threaded C)" % (passes, T, wl.T, total),
+        "us_per_call": total / passes * 1e6,
+        "us_layout": t_lay / passes * 1e6,
+        "us_dispatch": t_disp / passes * 1e6,
+        "us_combine": t_comb / passes * 1e6,
+    }
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    from oracle import build as oracle_build
+    oracle_build.build()
+    wl = W.WORKLOADS[args.workload]
+    tokens = 512
+    sub = wl.scaled(T=tokens)
+    x = W.bf16_bits(W.hidden_states(sub))
+    idx = W.route(sub).numpy()
+    w = W.topk_weights(sub).numpy()
+    for _ in range(args.warmup):
+        oracle_sample(wl, x, idx, w, tokens, 0.0)
+    vals, secs = [], 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = oracle_sample(wl, x, idx, w, tokens, 0.0)
+        vals.append(r["us_per_call"])
+    secs = time.perf_counter() - t0
+    disp_b, comb_b = sub.logical_bytes()
+    us = float(np.mean(vals))
+    value = (disp_b + comb_b) / (us * 1e-6) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.payload,
+        "data": "synthetic",
+        "config": {"workload": wl.name, "T_sampled": tokens, "T": wl.T, "H": wl.H, "E": wl.E,
+                   "k": wl.k, "R": wl.R, "layout": wl.kind, "payload": wl.payload,
+                   "route": wl.route, "zipf_s": wl.zipf_s},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step: layout+dispatch+combine of the first %d of %d "
+                                   "tokens (single-threaded C oracle); %.1f s total" % (
+                                       tokens, wl.T, secs)},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import combine_ep_layout_02_gb300 as ep
+    if not os.path.exists(ep.binding.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    ep.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.scaled(T=args.tokens, capacity=min(wl.capacity, args.tokens) or None)
+    torch.manual_seed(0)
+
+    # ---- inputs resident in HBM
+    x = W.hidden_states(wl, device=dev)
+    idx = W.route(wl, device=dev)
+    w = W.topk_weights(wl, device=dev)
+    lay = ep.LayoutOut(torch.empty(wl.E, dtype=torch.int32, device=dev),
+                       torch.empty(wl.E + 1, dtype=torch.int32, device=dev),
+                       torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev),
+                       torch.empty(wl.R, dtype=torch.int32, device=dev),
+                       torch.zeros(1, dtype=torch.int32, device=dev))
+    ws = torch.empty(max(16, ep.layout_workspace_bytes(wl.T, wl.k, wl.E, wl.R)), dtype=torch.uint8,
+                     device=dev)
+    if wl.payload == "fp8":
+        recv_q = torch.empty(wl.rows, wl.H, dtype=torch.uint8, device=dev)
+        recv_s = torch.empty(wl.rows, wl.H // 128, dtype=torch.float32, device=dev)
+    recv = None
+    if wl.payload == "bf16" or wl.expert_out == "recv":
+        recv = torch.empty(wl.rows, wl.H, dtype=torch.bfloat16, device=dev)
+    if wl.expert_out == "recv":
+        y = recv
+    elif wl.expert_out == "independent":
+        y = W.independent_expert_outputs(wl, device=dev)
+    else:
+        raise SystemExit("workload %s needs host-built expert outputs; not a bench workload" % wl.name)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
+        if ev:
+            ev[1].record(stream)
+        if wl.payload == "fp8":
+            ep.dispatch_fp8(x, lay.dst_row, wl.rows, recv_q=recv_q, recv_scale=recv_s,
+                            status=lay.status)
+        else:
+            ep.dispatch(x, lay.dst_row, wl.rows, recv=recv, status=lay.status)
+        if ev:
+            ev[2].record(stream)
+        ep.combine(y, w, lay.dst_row, out=out, status=lay.status)
+        if ev:
+            ev[3].record(stream)
+
+    # launches of our kernels per step: 3 layout kernels + dispatch + combine
+    launches_per_step = 5
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if ep.status_read(lay.status) != 0:
+        raise SystemExit("device status flags set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)  # let the sampler start
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world, dev)
+    total_ms = t_start.elapsed_time(t_end)
+    lay_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    disp_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    comb_ms = sum(e[2].elapsed_time(e[3]) for e in evs)
+    max_total_s = max_over_ranks(total_ms / 1e3, world, dev)
+    disp_b, comb_b = wl.logical_bytes()
+    logical = disp_b + comb_b
+    value = aggregate_value(logical, args.steps, max_total_s, world)
+    ms_per_step = max_total_s * 1e3 / args.steps
+
+    # ---- roofline of the dominant kernel (algorithmic bytes / event time)
+    Tk = wl.T * wl.k
+    alg = {
+        "layout": 2 * Tk * 4,
+        "dispatch": (wl.T * wl.H * 2 + Tk * wl.H * 2 + Tk * 4) if wl.payload == "bf16" else
+                    (wl.T * wl.H * 2 + Tk * (wl.H + wl.H // 32) + Tk * 4),
+        "combine": Tk * wl.H * 2 + wl.T * wl.H * 2 + Tk * 8,
+    }
+    per_launch_ms = {"layout": lay_ms / args.steps, "dispatch": disp_ms / args.steps,
+                     "combine": comb_ms / args.steps}
+    dominant = max(("dispatch", "combine"), key=lambda n: per_launch_ms[n])
+    peak, peak_src = measured_peak()
+    kname = "dispatch_fp8" if (dominant == "dispatch" and wl.payload == "fp8") else dominant
+
+    def roof(n):
+        a = alg[n] / (per_launch_ms[n] * 1e-3) / 1e9
+        return a, a / peak
+
+    ach, frac = roof(dominant)
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": frac, "peak_source": peak_src + " (%s)" % (
+                    "MEASURED_PEAKS.json hbm_gbs" if peak_src == "measured" else "6.8 TB/s"),
+                "algorithmic_bytes_per_launch": alg[dominant],
+                "traffic": ncu_traffic(kname, wl.name)}
+    kernels = {}
+    step_sum = sum(per_launch_ms.values())
+    for n in ("layout", "dispatch", "combine"):
+        a, f = roof(n)
+        kernels[n] = {"us_per_launch": per_launch_ms[n] * 1e3, "alg_bytes": alg[n],
+                      "achieved_GBs": a, "frac_of_peak": f, "share": per_launch_ms[n] / step_sum}
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        ih = idx.cpu().pin_memory()
+        wh = w.cpu().pin_memory()
+        oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+        x2 = torch.empty_like(x)
+        i2 = torch.empty_like(idx)
+        w2 = torch.empty_like(w)
+
+        def e2e_step():
+            x2.copy_(xh, non_blocking=True)
+            i2.copy_(ih, non_blocking=True)
+            w2.copy_(wh, non_blocking=True)
+            ep.layout(i2, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
+            if wl.payload == "fp8":
+                ep.dispatch_fp8(x2, lay.dst_row, wl.rows, recv_q=recv_q, recv_scale=recv_s,
+                                status=lay.status)
+            else:
+                ep.dispatch(x2, lay.dst_row, wl.rows, recv=recv, status=lay.status)
+            ep.combine(y, w2, lay.dst_row, out=out, status=lay.status)
+            oh.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b_ev.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(a_ev.elapsed_time(b_ev) / 1e3, world, dev)
+        if not torch.equal(oh.view(torch.int16), out.cpu().view(torch.int16)):
+            raise SystemExit("e2e output copy mismatch")
+        e2e = {"value": aggregate_value(logical, args.e2e_steps, e2e_s, world), "unit": "GB/s",
+               "ms_per_step": e2e_s * 1e3 / args.e2e_steps,
+               "h2d_bytes_per_step": x.numel() * 2 + idx.numel() * 4 + w.numel() * 4,
+               "d2h_bytes_per_step": out.numel() * 2}
+
+    if ep.status_read(lay.status) != 0:
+        raise SystemExit("device status flags set during the timed region")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tokens = 1024
+        cpu = oracle_sample(wl, W.bf16_bits(x[:tokens]), idx[:tokens].cpu().numpy(),
+                            w[:tokens].cpu().numpy(), tokens, args.cpu_seconds)
+
+    if rank == 0:
+        props = torch.cuda.get_device_properties(dev)
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.payload, "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k,
+                       "R": wl.R, "layout": wl.kind, "payload": wl.payload, "route": wl.route,
+                       "zipf_s": wl.zipf_s, "expert_outputs": wl.expert_out,
+                       "logical_bytes_per_step": logical,
+                       "l2": "inputs larger than L2 (x %.2f GB, dispatch buffer %.2f GB); no flush"
+                             % (x.numel() * 2 / 1e9, wl.rows * wl.H * (1 if wl.payload == 'fp8' else 2) / 1e9),
+                       "parallelism": "replicas x%d" % world},
+            "roofline": roofline,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "device": props.name,
+            "versions": {"torch": torch.__version__, "cuda": torch.version.cuda},
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) MoE expert-parallel hot path: routing layout, dispatch
+(BF16 or fused FP8 e4m3 with per-128-channel scales) and weighted top-k
+combine, as hand-written CUDA kernels behind a C ABI (``include/ep.h``).
+
+``binding`` marshals torch tensors into that ABI; ``workloads`` draws the
+seeded synthetic inputs.
+"""
+from .binding import (  # noqa: F401
+    EpError, LayoutOut, combine, dispatch, dispatch_fp8, layout, layout_workspace_bytes, load,
+    status_read, EP_FLAG_BAD_EXPERT, EP_FLAG_OVERFLOW, EP_FLAG_BAD_ROW,
+)

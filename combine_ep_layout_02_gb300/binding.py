@@ -1,0 +1,182 @@
+"""Thin ctypes binding over the C ABI in ``include/ep.h``.
+
+Argument marshalling only: every step of layout, dispatch and combine runs in
+the CUDA kernels of ``libep_gb300.so``.  Torch tensors supply device memory
+and the current CUDA stream.  If the library is missing this module raises;
+there is no fallback of any kind.
+"""
+import ctypes
+import os
+from collections import namedtuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libep_gb300.so")
+
+EP_OK = 0
+EP_ERR_INVALID_ARG = 1
+EP_ERR_ALIGNMENT = 2
+EP_ERR_WORKSPACE = 3
+EP_ERR_CUDA = 4
+
+EP_FLAG_BAD_EXPERT = 1
+EP_FLAG_OVERFLOW = 2
+EP_FLAG_BAD_ROW = 4
+
+LAYOUT_KINDS = {"contiguous": 0, "masked": 1}
+
+_lib = None
+
+
+class EpError(RuntimeError):
+    def __init__(self, fn, code):
+        lib = load()
+        msg = lib.ep_status_string(code).decode()
+        if code == EP_ERR_CUDA:
+            msg += " (cudaError %d)" % lib.ep_last_cuda_error()
+        super().__init__("%s failed: %s" % (fn, msg))
+        self.code = code
+
+
+def load():
+    """Load libep_gb300.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("CUDA library %s is not built; run __graft_entry__.build()" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "ep_version": ([], i32),
+        "ep_status_string": ([i32], ctypes.c_char_p),
+        "ep_last_cuda_error": ([], i32),
+        "ep_layout_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
+        "ep_layout": ([P, i64, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
+        "ep_dispatch": ([P, i64, i64, i32, P, P, i64, P, P], i32),
+        "ep_dispatch_fp8": ([P, i64, i64, i32, P, P, P, i64, P, P], i32),
+        "ep_combine": ([P, P, P, i64, i64, i32, i64, P, P, P], i32),
+        "ep_status_read": ([P, P, P], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_dev(name, t, dtype, device=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def _rc(fn, code):
+    if code != EP_OK:
+        raise EpError(fn, code)
+
+
+LayoutOut = namedtuple("LayoutOut", "expert_counts expert_offsets dst_row rank_token_counts status")
+
+
+def layout_workspace_bytes(T, k, E, R, with_rank_counts=True):
+    return int(load().ep_layout_workspace_bytes(T, k, E, R, 1 if with_rank_counts else 0))
+
+
+def layout(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=None, workspace=None,
+           with_rank_counts=True):
+    """Routing layout of ``topk_idx`` [T, k] int32 (see ``ep_layout``)."""
+    _check_dev("topk_idx", topk_idx, torch.int32)
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    if out is None:
+        out = LayoutOut(
+            torch.empty(E, dtype=torch.int32, device=dev),
+            torch.empty(E + 1, dtype=torch.int32, device=dev),
+            torch.empty(T, k, dtype=torch.int32, device=dev),
+            torch.empty(R, dtype=torch.int32, device=dev) if with_rank_counts else None,
+            torch.empty(1, dtype=torch.int32, device=dev),
+        )
+    need = layout_workspace_bytes(T, k, E, R, out.rank_token_counts is not None)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    code = load().ep_layout(_ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity,
+                            _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.dst_row),
+                            _ptr(out.rank_token_counts), _ptr(out.status), _ptr(workspace), wbytes,
+                            _stream(dev))
+    _rc("ep_layout", code)
+    return out
+
+
+def dispatch(x, dst_row, rows, recv=None, status=None):
+    """BF16 dispatch of ``x`` [T, H] into ``recv`` [rows, H] (see ``ep_dispatch``)."""
+    _check_dev("x", x, torch.bfloat16)
+    _check_dev("dst_row", dst_row, torch.int32, x.device)
+    T, H = x.shape
+    k = dst_row.shape[1]
+    if recv is None:
+        recv = torch.empty(rows, H, dtype=torch.bfloat16, device=x.device)
+    _check_dev("recv", recv, torch.bfloat16, x.device)
+    code = load().ep_dispatch(_ptr(x), T, H, k, _ptr(dst_row), _ptr(recv), rows, _ptr(status),
+                              _stream(x.device))
+    _rc("ep_dispatch", code)
+    return recv
+
+
+def dispatch_fp8(x, dst_row, rows, recv_q=None, recv_scale=None, status=None):
+    """FP8 e4m3 dispatch with fused per-128-channel scaling (see ``ep_dispatch_fp8``).
+    Returns (recv_q uint8 [rows, H], recv_scale float32 [rows, H/128])."""
+    _check_dev("x", x, torch.bfloat16)
+    _check_dev("dst_row", dst_row, torch.int32, x.device)
+    T, H = x.shape
+    k = dst_row.shape[1]
+    if recv_q is None:
+        recv_q = torch.empty(rows, H, dtype=torch.uint8, device=x.device)
+    if recv_scale is None:
+        recv_scale = torch.empty(rows, H // 128, dtype=torch.float32, device=x.device)
+    _check_dev("recv_q", recv_q, torch.uint8, x.device)
+    _check_dev("recv_scale", recv_scale, torch.float32, x.device)
+    code = load().ep_dispatch_fp8(_ptr(x), T, H, k, _ptr(dst_row), _ptr(recv_q), _ptr(recv_scale),
+                                  rows, _ptr(status), _stream(x.device))
+    _rc("ep_dispatch_fp8", code)
+    return recv_q, recv_scale
+
+
+def combine(y, topk_w, dst_row, out=None, status=None):
+    """Weighted top-k combine of ``y`` [rows, H] into ``out`` [T, H] (see ``ep_combine``)."""
+    _check_dev("y", y, torch.bfloat16)
+    _check_dev("topk_w", topk_w, torch.float32, y.device)
+    _check_dev("dst_row", dst_row, torch.int32, y.device)
+    rows, H = y.shape
+    T, k = dst_row.shape
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=y.device)
+    _check_dev("out", out, torch.bfloat16, y.device)
+    code = load().ep_combine(_ptr(y), _ptr(topk_w), _ptr(dst_row), T, H, k, rows, _ptr(out),
+                             _ptr(status), _stream(y.device))
+    _rc("ep_combine", code)
+    return out
+
+
+def status_read(status):
+    """Synchronise the current stream and return the device status word."""
+    flags = ctypes.c_uint32(0)
+    code = load().ep_status_read(_ptr(status), _stream(status.device), ctypes.byref(flags))
+    _rc("ep_status_read", code)
+    return int(flags.value)

@@ -1,0 +1,130 @@
+// ep_api.cu -- the C ABI: argument validation on the host, then the launches.
+// Every check that can fail happens before anything is enqueued.
+#include <stdint.h>
+
+#include "ep_internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return EP_OK;
+    g_last_cuda_error = (int)e;
+    return EP_ERR_CUDA;
+}
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Common checks of (T, H, k, rows) for dispatch and combine.
+int check_rows_args(int64_t T, int64_t H, int k, int64_t rows) {
+    if (T < 0 || H <= 0 || k < 1 || k > EP_MAX_TOPK || rows < 0) return EP_ERR_INVALID_ARG;
+    if (T > 0 && T > (int64_t)INT32_MAX / k) return EP_ERR_INVALID_ARG;
+    if (rows > (int64_t)INT32_MAX + 1) return EP_ERR_INVALID_ARG;
+    if (H % 8 != 0) return EP_ERR_ALIGNMENT;
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_version(void) { return (1 << 16) | 0; }
+
+const char* ep_status_string(int status) {
+    switch (status) {
+        case EP_OK: return "EP_OK";
+        case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+        case EP_ERR_ALIGNMENT: return "EP_ERR_ALIGNMENT";
+        case EP_ERR_WORKSPACE: return "EP_ERR_WORKSPACE";
+        case EP_ERR_CUDA: return "EP_ERR_CUDA";
+        default: return "EP_ERR_UNKNOWN";
+    }
+}
+
+int ep_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t ep_layout_workspace_bytes(int64_t T, int k, int E, int R, int with_rank_counts) {
+    if (T <= 0 || k < 1 || E < 1 || R < 1) return 0;
+    const int64_t nchunk = ep::layout_num_chunks(T);
+    const int64_t cols = E + (with_rank_counts ? R : 0);
+    const size_t bytes = (size_t)(nchunk * cols) * sizeof(int32_t);
+    return (bytes + 255) & ~(size_t)255;
+}
+
+int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind, int capacity,
+              int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+              int32_t* rank_token_counts, uint32_t* status, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    if (T < 0 || k < 1 || k > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || E % R != 0)
+        return EP_ERR_INVALID_ARG;
+    if (T > (int64_t)INT32_MAX / k) return EP_ERR_INVALID_ARG;
+    if (kind != EP_LAYOUT_CONTIGUOUS && kind != EP_LAYOUT_MASKED) return EP_ERR_INVALID_ARG;
+    if (kind == EP_LAYOUT_MASKED && (capacity < 0 || (int64_t)E * capacity > (int64_t)INT32_MAX))
+        return EP_ERR_INVALID_ARG;
+    if (!expert_counts || !expert_offsets) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !dst_row)) return EP_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 4) || !aligned(dst_row, 4) || !aligned(expert_counts, 4) ||
+        !aligned(expert_offsets, 4) || !aligned(rank_token_counts, 4) || !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    const size_t need = ep_layout_workspace_bytes(T, k, E, R, rank_token_counts != nullptr);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return EP_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return EP_ERR_ALIGNMENT;
+    }
+    return cuda_status(ep::launch_layout(topk_idx, T, k, E, R, kind, capacity, expert_counts,
+                                         expert_offsets, dst_row, rank_token_counts, status,
+                                         static_cast<int32_t*>(workspace), as_stream(stream)));
+}
+
+int ep_dispatch(const void* x, int64_t T, int64_t H, int k, const int32_t* dst_row, void* recv,
+                int64_t rows, uint32_t* status, void* stream) {
+    int rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (T == 0) return EP_OK;
+    if (!x || !dst_row || (!recv && rows > 0)) return EP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(dst_row, 4) || !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(
+        ep::launch_dispatch_bf16(x, T, H, k, dst_row, recv, rows, status, as_stream(stream)));
+}
+
+int ep_dispatch_fp8(const void* x, int64_t T, int64_t H, int k, const int32_t* dst_row,
+                    uint8_t* recv_q, float* recv_scale, int64_t rows, uint32_t* status,
+                    void* stream) {
+    int rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (H % 128 != 0) return EP_ERR_ALIGNMENT;
+    if (T == 0) return EP_OK;
+    if (!x || !dst_row || ((!recv_q || !recv_scale) && rows > 0)) return EP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv_q, 16) || !aligned(recv_scale, 4) ||
+        !aligned(dst_row, 4) || !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(ep::launch_dispatch_fp8(x, T, H, k, dst_row, recv_q, recv_scale, rows,
+                                               status, as_stream(stream)));
+}
+
+int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row, int64_t T, int64_t H,
+               int k, int64_t rows, void* out, uint32_t* status, void* stream) {
+    int rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (T == 0) return EP_OK;
+    if (!topk_w || !dst_row || !out || (!y && rows > 0)) return EP_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_w, 4) || !aligned(dst_row, 4) ||
+        !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(ep::launch_combine(y, topk_w, dst_row, T, H, k, rows, out, status,
+                                          as_stream(stream)));
+}
+
+int ep_status_read(const uint32_t* status, void* stream, uint32_t* host_flags) {
+    if (!status || !host_flags) return EP_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyAsync(host_flags, status, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                    as_stream(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+    return cuda_status(e);
+}
+
+}  // extern "C"

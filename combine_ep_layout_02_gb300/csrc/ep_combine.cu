@@ -1,0 +1,106 @@
+// ep_combine.cu -- weighted top-k combine: out[t] = bf16(sum_j w[t,j] *
+// y[dst_row[t,j]]), accumulated in fp32 fused multiply-adds in increasing j.
+//
+// One warp per token.  Per iteration each lane owns 8 channels (one 16-byte
+// vector) of U column groups; the loads of all k rows for those groups are
+// issued before any arithmetic so that k*U 16-byte loads per lane are in
+// flight, then the FMAs run in j order (the order fixes the fp32 result
+// bit-for-bit).  Every expert-output byte is read once and every output byte
+// written once: T*k*H*2 read + T*H*2 written is the HBM floor.
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kCombineWarps = 8;
+constexpr int kRowBatch = 8;  // rows whose loads are issued together
+
+template <int U>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
+               const int32_t* __restrict__ dst_row, int64_t T, int64_t nvec, int k, int64_t rows,
+               uint4* __restrict__ out, uint32_t* __restrict__ status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    if (t >= T) return;  // warp-uniform
+
+    int my_row = -1;
+    float my_w = 0.0f;
+    bool bad = false;
+    if (lane < k) {
+        my_row = __ldg(dst_row + t * k + lane);
+        my_w = __ldg(topk_w + t * k + lane);
+        if (my_row < -1 || (int64_t)my_row >= rows) {
+            bad = true;
+            my_row = -1;
+        }
+    }
+    warp_flag(status, bad, EP_FLAG_BAD_ROW);
+
+    for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+        float acc[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+
+        for (int j0 = 0; j0 < k; j0 += kRowBatch) {
+            uint4 buf[kRowBatch][U];
+            int rr[kRowBatch];
+#pragma unroll
+            for (int jj = 0; jj < kRowBatch; ++jj) {
+                const int j = j0 + jj;
+                rr[jj] = __shfl_sync(kFullMask, my_row, j & 31);
+                if (j >= k) rr[jj] = -1;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = v0 + u * 32 + lane;
+                    buf[jj][u] = make_uint4(0, 0, 0, 0);
+                    if (rr[jj] >= 0 && v < nvec) buf[jj][u] = ld_stream_v4(y + (int64_t)rr[jj] * nvec + v);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < kRowBatch; ++jj) {
+                const float w = __shfl_sync(kFullMask, my_w, (j0 + jj) & 31);
+                if (rr[jj] < 0) continue;  // warp-uniform: skipped pairs add nothing
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t wv[4] = {buf[jj][u].x, buf[jj][u].y, buf[jj][u].z, buf[jj][u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[u][2 * i] = __fmaf_rn(w, bf16lo_to_f32(wv[i]), acc[u][2 * i]);
+                        acc[u][2 * i + 1] = __fmaf_rn(w, bf16hi_to_f32(wv[i]), acc[u][2 * i + 1]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * 32 + lane;
+            if (v < nvec) {
+                uint4 o;
+                o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
+                o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
+                o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
+                o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
+                st_v4(out + t * nvec + v, o);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* dst_row, int64_t T,
+                           int64_t H, int k, int64_t rows, void* out, uint32_t* status,
+                           cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int64_t nvec = H / 8;
+    const unsigned grid = (unsigned)((T + kCombineWarps - 1) / kCombineWarps);
+    combine_kernel<2><<<grid, kCombineWarps * 32, 0, stream>>>(
+        static_cast<const uint4*>(y), topk_w, dst_row, T, nvec, k, rows,
+        static_cast<uint4*>(out), status);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

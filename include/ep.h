@@ -1,0 +1,185 @@
+/*
+ * ep.h -- C ABI of the GB300 (sm_103a) MoE expert-parallel hot path:
+ * routing layout, dispatch (BF16 or FP8 e4m3 with per-128-channel scales)
+ * and weighted top-k combine, all on one GPU.
+ *
+ * The operations are the local steps of DeepEP-style dispatch/combine as the
+ * pages state the problem ("Replace EP backend comparison with Decode-like
+ * and Prefill-like B200 benchmarks", awsome-distributed-ai PR #1238, section
+ * "What changed": BF16 input with an exact top-k route and weights; FP8
+ * conversion, the dispatch layout, dispatch and combine inside one timed
+ * boundary; and the afdEP-comm validation record, "setup": masked
+ * [experts, capacity, hidden] buffers with capacity 2048).  "Virtual ranks"
+ * are only a grouping of experts here: rank r owns experts
+ * [r*E/R, (r+1)*E/R).  There is no communication.
+ *
+ * Conventions for every call
+ *  - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
+ *    (allocates and frees) every buffer; the library allocates nothing.
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Every call only enqueues work on `stream` and returns; nothing
+ *    synchronises except ep_status_read().
+ *  - Return value: an ep_status_t.  A non-zero value detected on the host
+ *    (bad sizes, NULL or misaligned pointers, small workspace) means that
+ *    NOTHING was enqueued.  EP_ERR_CUDA means a launch failed (the CUDA error
+ *    is available from ep_last_cuda_error()).
+ *  - Conditions found on the device never trap: they are OR-ed as EP_FLAG_*
+ *    bits into the optional `status` word (a device uint32), which the caller
+ *    reads with ep_status_read().  ep_layout() zeroes the word first;
+ *    ep_dispatch*() and ep_combine() only OR into it.
+ *  - bf16 tensors are passed as raw 16-bit patterns, row-major.
+ *  - dst_row[t*k + j] is the row of the dispatch buffer that receives token t
+ *    for its j-th expert, or -1 when the pair is not routed (expert id -1, a
+ *    bad id, or a masked-capacity overflow).  Pairs with dst_row == -1 are
+ *    skipped by dispatch and contribute nothing to combine.
+ *
+ * Limits: 1 <= k <= EP_MAX_TOPK; 1 <= E <= EP_MAX_EXPERTS; R >= 1 divides E;
+ * T*k < 2^31; E*capacity < 2^31 (masked); H % 8 == 0 (BF16 rows are whole
+ * 16-byte vectors); H % 128 == 0 for FP8; 16-byte-aligned bf16/e4m3 buffers.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define EP_API __attribute__((visibility("default")))
+#else
+#define EP_API
+#endif
+
+#define EP_MAX_TOPK 32
+#define EP_MAX_EXPERTS 1024
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1, /* NULL pointer, size out of range, E % R != 0 ... */
+    EP_ERR_ALIGNMENT = 2,   /* H or a pointer violates the alignment rules     */
+    EP_ERR_WORKSPACE = 3,   /* workspace smaller than ep_layout_workspace_bytes */
+    EP_ERR_CUDA = 4         /* a kernel launch or copy failed                   */
+} ep_status_t;
+
+/* Device-side condition bits (OR-ed into *status). */
+enum {
+    EP_FLAG_BAD_EXPERT = 1u, /* an expert id outside [-1, E): the pair was skipped */
+    EP_FLAG_OVERFLOW = 2u,   /* masked layout: slot >= capacity, the pair was dropped */
+    EP_FLAG_BAD_ROW = 4u     /* dispatch/combine: dst_row outside [-1, rows): skipped */
+};
+
+typedef enum { EP_LAYOUT_CONTIGUOUS = 0, EP_LAYOUT_MASKED = 1 } ep_layout_kind_t;
+
+/* Library version, (major << 16) | minor. */
+EP_API int ep_version(void);
+
+/* Human-readable name of an ep_status_t. Never NULL. */
+EP_API const char* ep_status_string(int status);
+
+/* The CUDA error (cudaError_t as int) of the last EP_ERR_CUDA on this host
+ * thread, 0 if none. */
+EP_API int ep_last_cuda_error(void);
+
+/* Bytes of device workspace ep_layout() needs for these sizes (0 when T == 0).
+ * with_rank_counts: non-zero if rank_token_counts will be requested. */
+EP_API size_t ep_layout_workspace_bytes(int64_t T, int k, int E, int R, int with_rank_counts);
+
+/*
+ * ep_layout -- routing layout: per-expert counts, exclusive scan, stable slot.
+ * (PR #1238 "What changed": the Prefill-like profile includes the dispatch
+ * layout the normal API requires; masked buffers from the afdEP "setup".)
+ *
+ *  topk_idx          [T, k] int32 expert ids; -1 = no expert.
+ *  kind, capacity    EP_LAYOUT_CONTIGUOUS (capacity ignored) or
+ *                    EP_LAYOUT_MASKED with `capacity` rows per expert.
+ *  expert_counts     [E] int32 out: pairs routed to each expert (the true
+ *                    count, also when a masked expert overflows).
+ *  expert_offsets    [E+1] int32 out: exclusive scan of expert_counts;
+ *                    expert_offsets[E] = rows used by the contiguous layout.
+ *  dst_row           [T, k] int32 out.  A pair's slot is the number of
+ *                    earlier pairs (in flattened order t*k+j) with the same
+ *                    expert.  Contiguous: expert_offsets[e] + slot.
+ *                    Masked: e*capacity + slot, or -1 with EP_FLAG_OVERFLOW
+ *                    when slot >= capacity.  Ids outside [-1, E) give -1 and
+ *                    EP_FLAG_BAD_EXPERT.
+ *  rank_token_counts [R] int32 out or NULL: tokens with at least one valid
+ *                    expert in virtual rank r.
+ *  status            [1] uint32 or NULL: zeroed, then device flags OR-ed in.
+ *  workspace         device scratch of at least
+ *                    ep_layout_workspace_bytes(T, k, E, R, rank_token_counts != NULL)
+ *                    bytes, 16-byte aligned; contents need no initialisation
+ *                    and are clobbered.  May be NULL when that size is 0.
+ * T == 0 is valid: counts, offsets and rank counts are written as zeros.
+ */
+EP_API int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+              int kind, int capacity,
+              int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+              int32_t* rank_token_counts, uint32_t* status,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ep_dispatch -- BF16 dispatch (scatter): recv[dst_row[t,j], :] = x[t, :],
+ * a bit copy (PR #1238 "What changed": each token is sent to its top-k
+ * experts; the BF16 payload is T*k*H*2 bytes).
+ *
+ *  x        [T, H] bf16, 16-byte aligned.
+ *  dst_row  [T, k] int32 from ep_layout.
+ *  recv     [rows, H] bf16, 16-byte aligned.  Rows no pair maps to (masked
+ *           padding, rows past expert_offsets[E]) are not touched.
+ *  rows     number of rows of recv; a dst_row outside [-1, rows) is skipped
+ *           and raises EP_FLAG_BAD_ROW.
+ */
+EP_API int ep_dispatch(const void* x, int64_t T, int64_t H, int k, const int32_t* dst_row,
+                void* recv, int64_t rows, uint32_t* status, void* stream);
+
+/*
+ * ep_dispatch_fp8 -- dispatch with the per-token FP8 cast fused into the copy
+ * (PR #1238: the standalone cast is a separate launch-bound step in the
+ * timed boundary; the low-latency API quantises inside the dispatch kernel;
+ * the payload carries one float32 scale per 128 channels).  For each token t
+ * and block b of 128 channels:
+ *     a   = max |x[t, 128b .. 128b+127]|         (fp32)
+ *     a'  = max(a, 1e-4f)
+ *     sf  = a' / 448.0f                          (IEEE fp32 division, RNE)
+ *     inv = 448.0f / a'                          (IEEE fp32 division, RNE)
+ *     q   = e4m3(x * inv)   fp32 product rounded to nearest even, then
+ *                           e4m3 "fn" with round-to-nearest-even and
+ *                           saturation to +-448
+ * q and sf are written to every dst_row of the token; x ~= e4m3_value(q) * sf.
+ *
+ *  recv_q      [rows, H] uint8 e4m3 codes, 16-byte aligned.
+ *  recv_scale  [rows, H/128] float32, row-major, 4-byte aligned.
+ *  H % 128 == 0 is required.
+ */
+EP_API int ep_dispatch_fp8(const void* x, int64_t T, int64_t H, int k, const int32_t* dst_row,
+                    uint8_t* recv_q, float* recv_scale, int64_t rows,
+                    uint32_t* status, void* stream);
+
+/*
+ * ep_combine -- weighted top-k reduction back into token order (the combine
+ * step of the PR's timed boundary; BF16 in either payload mode):
+ *     out[t, h] = bf16_rne( sum over j with dst_row[t,j] != -1 of
+ *                           topk_w[t,j] * y[dst_row[t,j], h] )
+ * accumulated in fp32 as fused multiply-adds in increasing j, starting from
+ * +0, then rounded to bf16 (nearest even).  A token with no valid pair
+ * gives +0.
+ *
+ *  y        [rows, H] bf16 expert outputs in the dispatch layout, 16-byte aligned.
+ *  topk_w   [T, k] float32 top-k weights.
+ *  out      [T, H] bf16, 16-byte aligned; must not overlap y.
+ */
+EP_API int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row,
+               int64_t T, int64_t H, int k, int64_t rows, void* out,
+               uint32_t* status, void* stream);
+
+/* Copy the device status word to *host_flags (a HOST pointer) after
+ * synchronising `stream`. */
+EP_API int ep_status_read(const uint32_t* status, void* stream, uint32_t* host_flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EP_GB300_H */

@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads and exports every symbol that
+include/ep.h declares; host-side argument validation rejects bad calls
+before anything is enqueued (no GPU needed for any of this)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from combine_ep_layout_02_gb300 import build as cuda_build
+    cuda_build.build()
+    from combine_ep_layout_02_gb300 import binding
+    return binding.load()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        with open(os.path.join(ROOT, "include", fn)) as f:
+            text = f.read()
+        names += re.findall(r"^EP_API\s+[\w\s\*]+?\b(ep_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for required in ("ep_layout", "ep_dispatch", "ep_dispatch_fp8", "ep_combine"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ep_version() >> 16 == 1
+    assert lib.ep_status_string(0) == b"EP_OK"
+    assert lib.ep_status_string(3) == b"EP_ERR_WORKSPACE"
+    assert lib.ep_status_string(99) == b"EP_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    assert lib.ep_layout_workspace_bytes(0, 8, 256, 16, 1) == 0
+    # 65536 tokens -> 128 chunks of 512; (256 + 16) columns of int32
+    assert lib.ep_layout_workspace_bytes(65536, 8, 256, 16, 1) == 128 * 272 * 4
+    assert lib.ep_layout_workspace_bytes(65536, 8, 256, 16, 0) == 128 * 256 * 4
+    assert lib.ep_layout_workspace_bytes(1, 8, 3, 1, 0) == 256   # rounded up to 256 bytes
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation
+
+
+def test_layout_argument_validation(lib):
+    def call(T=16, k=8, E=256, R=16, kind=0, cap=0, ws=FAKE, wsb=1 << 30, idx=FAKE, cnt=FAKE,
+             off=FAKE, dst=FAKE):
+        return lib.ep_layout(idx, T, k, E, R, kind, cap, cnt, off, dst, None, None, ws, wsb, None)
+    assert call(E=255) == 1           # E % R != 0
+    assert call(k=0) == 1
+    assert call(k=33) == 1
+    assert call(E=2048, R=1) == 1     # E > EP_MAX_EXPERTS
+    assert call(T=-1) == 1
+    assert call(kind=7) == 1
+    assert call(kind=1, cap=-1) == 1
+    assert call(kind=1, cap=1 << 24) == 1      # E * capacity >= 2^31
+    assert call(cnt=None) == 1
+    assert call(idx=None) == 1
+    assert call(ws=None) == 3
+    assert call(wsb=16) == 3
+    assert call(idx=ctypes.c_void_p((1 << 20) + 2)) == 2
+    assert call(ws=ctypes.c_void_p((1 << 20) + 4)) == 2
+
+
+def test_dispatch_combine_argument_validation(lib):
+    assert lib.ep_dispatch(FAKE, 4, 100, 8, FAKE, FAKE, 32, None, None) == 2        # H % 8
+    assert lib.ep_dispatch(FAKE, 4, 64, 0, FAKE, FAKE, 32, None, None) == 1          # k
+    assert lib.ep_dispatch(None, 4, 64, 8, FAKE, FAKE, 32, None, None) == 1
+    assert lib.ep_dispatch(ctypes.c_void_p((1 << 20) + 8), 4, 64, 8, FAKE, FAKE, 32, None, None) == 2
+    assert lib.ep_dispatch(FAKE, 0, 64, 8, FAKE, FAKE, 32, None, None) == 0          # T == 0: no-op
+    assert lib.ep_dispatch_fp8(FAKE, 4, 64, 8, FAKE, FAKE, FAKE, 32, None, None) == 2  # H % 128
+    assert lib.ep_dispatch_fp8(FAKE, 4, 256, 8, FAKE, FAKE, ctypes.c_void_p((1 << 20) + 2), 32,
+                               None, None) == 2
+    assert lib.ep_combine(FAKE, FAKE, FAKE, 4, 64, 8, 32, None, None, None) == 1      # out NULL
+    assert lib.ep_combine(FAKE, FAKE, FAKE, 4, 60, 8, 32, FAKE, None, None) == 2
+    assert lib.ep_combine(FAKE, FAKE, FAKE, -1, 64, 8, 32, FAKE, None, None) == 1
+    assert lib.ep_status_read(None, None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from combine_ep_layout_02_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load()

@@ -1,0 +1,70 @@
+"""Host-side logic of bench.py: the max-over-ranks reduction and the
+whole-job aggregation on world_size-2 gloo process groups (CPU), and the
+CPU-only reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local_seconds = 1.0 + rank          # rank 1 is the slowest
+    m = bench.max_over_ranks(local_seconds, world)
+    bench.barrier(world)
+    v = bench.aggregate_value(15e9, 10, m, world)
+    q.put((rank, m, v))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_aggregate_gloo():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, m, v in res:
+        assert m == 2.0                                   # max over ranks
+        assert v == pytest.approx(2 * 15e9 * 10 / 2.0 / 1e9)  # all ranks' bytes / slowest time
+
+
+def test_single_rank_helpers():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.aggregate_value(1e9, 4, 2.0, 1) == pytest.approx(2.0)
+    peak, src = bench.measured_peak()
+    assert peak > 0 and src in ("measured", "fallback")
+
+
+def test_reference_arm_runs_on_cpu():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
