@@ -54,6 +54,7 @@ def load():
         "ep_last_cuda_error": ([], i32),
         "ep_layout_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
         "ep_layout": ([P, i64, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
+        "ep_layout_static_ws": ([P, i64, i32, i32, i32, i32, i32, P, P, P, P, P, P], i32),
         "ep_dispatch": ([P, i64, i64, i32, P, P, i64, P, P], i32),
         "ep_dispatch_fp8": ([P, i64, i64, i32, P, P, P, i64, P, P], i32),
         "ep_combine": ([P, P, P, i64, i64, i32, i64, P, P, P], i32),
@@ -121,6 +122,31 @@ def layout(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=None, workspa
                             _ptr(out.rank_token_counts), _ptr(out.status), _ptr(workspace), wbytes,
                             _stream(dev))
     _rc("ep_layout", code)
+    return out
+
+
+def layout_static_ws(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=None,
+                     with_rank_counts=True):
+    """Routing layout through ``ep_layout_static_ws``: the same result as
+    ``layout`` without any workspace, for callers that cannot allocate device
+    memory.  The outputs must still be passed in (``out``) by such callers;
+    when ``out`` is None they are allocated here for convenience."""
+    _check_dev("topk_idx", topk_idx, torch.int32)
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    if out is None:
+        out = LayoutOut(
+            torch.empty(E, dtype=torch.int32, device=dev),
+            torch.empty(E + 1, dtype=torch.int32, device=dev),
+            torch.empty(T, k, dtype=torch.int32, device=dev),
+            torch.empty(R, dtype=torch.int32, device=dev) if with_rank_counts else None,
+            torch.empty(1, dtype=torch.int32, device=dev),
+        )
+    code = load().ep_layout_static_ws(_ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity,
+                                      _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                      _ptr(out.dst_row), _ptr(out.rank_token_counts),
+                                      _ptr(out.status), _stream(dev))
+    _rc("ep_layout_static_ws", code)
     return out
 
 

@@ -29,6 +29,10 @@ int check_rows_args(int64_t T, int64_t H, int k, int64_t rows) {
 
 }  // namespace
 
+namespace ep {
+void record_cuda_error(int err) { g_last_cuda_error = err; }
+}  // namespace ep
+
 extern "C" {
 
 int ep_version(void) { return (1 << 16) | 0; }

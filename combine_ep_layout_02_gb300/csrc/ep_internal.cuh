@@ -71,6 +71,9 @@ __device__ __forceinline__ void warp_flag(uint32_t* status, bool cond, uint32_t 
 
 // ---- launchers (host) ------------------------------------------------------
 
+// Record a CUDA error for ep_last_cuda_error() (host, per thread).
+void record_cuda_error(int err);
+
 // Tokens per layout chunk (one per thread of a 512-thread block).
 constexpr int kLayoutThreads = 512;
 constexpr int kLayoutWarps = kLayoutThreads / 32;

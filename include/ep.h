@@ -55,6 +55,7 @@ extern "C" {
 
 #define EP_MAX_TOPK 32
 #define EP_MAX_EXPERTS 1024
+#define EP_STATIC_WS_BYTES (2u << 20) /* scratch held by ep_layout_static_ws() */
 
 typedef enum {
     EP_OK = 0,
@@ -119,6 +120,38 @@ EP_API int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
               int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
               int32_t* rank_token_counts, uint32_t* status,
               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ep_layout_static_ws -- ep_layout() for callers that cannot allocate device
+ * memory: for example a plug-in whose host application owns all device
+ * memory through its own pool and gives the plug-in no way to allocate, or a
+ * real-time loop that must not allocate once it is running.  The pages have
+ * no counterpart; this call exists only for such callers.
+ *
+ * Arguments, outputs and status are those of ep_layout(), minus the
+ * workspace: the layout's scratch is one fixed array of EP_STATIC_WS_BYTES
+ * (2 MiB) in the library's own device memory, which every GPU that loads the
+ * library holds until the process exits.
+ *  - Returns EP_ERR_WORKSPACE, enqueueing nothing, when
+ *    ep_layout_workspace_bytes(T, k, E, R, rank_token_counts != NULL) exceeds
+ *    EP_STATIC_WS_BYTES.  (Example: T = 131072, E = 256, R = 32 needs 0.29 MB;
+ *    the limit is about 512k int32 counters of (E+R) x ceil(T/512).)
+ *  - The first call on a device looks up the array's device address, with
+ *    the caller's current device; that device must be the one `stream`
+ *    belongs to.  Make the first call on each device before any stream
+ *    capture begins.
+ *  - Every call on a device shares the one array, and it keeps the last
+ *    call's contents (the layout fully rewrites what it reads, so nothing
+ *    needs clearing).  Calls whose kernels overlap on the GPU (for example
+ *    on two streams without an event between them) race on it and produce
+ *    wrong layouts: serialise them.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+EP_API int ep_layout_static_ws(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                               int kind, int capacity,
+                               int32_t* expert_counts, int32_t* expert_offsets,
+                               int32_t* dst_row, int32_t* rank_token_counts,
+                               uint32_t* status, void* stream);
 
 /*
  * ep_dispatch -- BF16 dispatch (scatter): recv[dst_row[t,j], :] = x[t, :],
