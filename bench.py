@@ -56,10 +56,14 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0,
                     help="scale the workload to this many tokens (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--chunk-tokens", type=int, default=4096,
+                    help="token chunk of the host-buffer executor (e2e)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the timed oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the step as one captured CUDA graph (launch-bound small shapes)")
     return ap.parse_args()
 
 
@@ -298,8 +302,13 @@ def run_ours(args, rank, world, local):
         y = recv
     elif wl.expert_out == "independent":
         y = W.independent_expert_outputs(wl, device=dev)
-    else:
-        raise SystemExit("workload %s needs host-built expert outputs; not a bench workload" % wl.name)
+    else:  # scaled_recv: expert outputs = dispatched rows x per-expert scale
+        lay0 = ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity)
+        r0 = ep.dispatch(x, lay0.dst_row, wl.rows)
+        row_expert = torch.full((wl.rows,), -1, dtype=torch.int64, device=dev)
+        row_expert[lay0.dst_row.view(-1).long()] = idx.view(-1).long()
+        y = W.scale_rows(r0, row_expert, W.expert_scales(wl, device=dev))
+        del r0, lay0
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -326,10 +335,19 @@ def run_ours(args, rank, world, local):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
+    run_step = step
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        run_step = graph.replay
     if ep.status_read(lay.status) != 0:
         raise SystemExit("device status flags set during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # timed region: K steps between one event pair, nothing else on the stream
+    # (so consecutive kernels keep their programmatic-dependent-launch overlap)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world, dev)
@@ -337,13 +355,20 @@ def run_ours(args, rank, world, local):
     sampler = ClockSampler(local)
     time.sleep(0.3)  # let the sampler start
     t_start.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
+    for _ in range(args.steps):
+        run_step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(world, dev)
     total_ms = t_start.elapsed_time(t_end)
+
+    # per-kernel times: the same K steps again with an event pair around each
+    # call (events between kernels, so no launch overlap at those boundaries)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
     lay_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
     disp_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
     comb_ms = sum(e[2].elapsed_time(e[3]) for e in evs)
@@ -372,7 +397,8 @@ def run_ours(args, rank, world, local):
         return a, a / peak
 
     ach, frac = roof(dominant)
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": ach, "peak": peak, "unit": "GB/s",
+    roofline = {"bound": "hbm", "kernel": kname,
+                "timing": "CUDA events around each call over a second pass of the K steps", "achieved": ach, "peak": peak, "unit": "GB/s",
                 "frac": frac, "peak_source": peak_src + " (%s)" % (
                     "MEASURED_PEAKS.json hbm_gbs" if peak_src == "measured" else "6.8 TB/s"),
                 "algorithmic_bytes_per_launch": alg[dominant],
@@ -384,47 +410,43 @@ def run_ours(args, rank, world, local):
         kernels[n] = {"us_per_launch": per_launch_ms[n] * 1e3, "alg_bytes": alg[n],
                       "achieved_GBs": a, "frac_of_peak": f, "share": per_launch_ms[n] / step_sum}
 
-    # ---- end to end through the public API with pinned host buffers
+    # ---- end to end through the public API with pinned host buffers: the
+    # host-buffer executor (ep_roundtrip_host) copies the route, runs the
+    # layout, streams x in token chunks overlapped with dispatch + combine, and
+    # streams the output back, all inside the timed region
     e2e = None
     if not args.no_e2e:
         xh = x.cpu().pin_memory()
         ih = idx.cpu().pin_memory()
         wh = w.cpu().pin_memory()
         oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
-        x2 = torch.empty_like(x)
-        i2 = torch.empty_like(idx)
-        w2 = torch.empty_like(w)
-
-        def e2e_step():
-            x2.copy_(xh, non_blocking=True)
-            i2.copy_(ih, non_blocking=True)
-            w2.copy_(wh, non_blocking=True)
-            ep.layout(i2, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
-            if wl.payload == "fp8":
-                ep.dispatch_fp8(x2, lay.dst_row, wl.rows, recv_q=recv_q, recv_scale=recv_s,
-                                status=lay.status)
-            else:
-                ep.dispatch(x2, lay.dst_row, wl.rows, recv=recv, status=lay.status)
-            ep.combine(y, w2, lay.dst_row, out=out, status=lay.status)
-            oh.copy_(out, non_blocking=True)
-
+        pipe = ep.Pipeline(wl.T, wl.H, wl.k, wl.E, wl.R, wl.kind, wl.capacity,
+                           chunk_tokens=args.chunk_tokens, device=dev,
+                           y=None if wl.expert_out == "recv" else y)
         for _ in range(3):
-            e2e_step()
+            pipe.run(xh, ih, wh, oh)
         torch.cuda.synchronize(dev)
         barrier(world, dev)
         a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a_ev.record(stream)
         for _ in range(args.e2e_steps):
-            e2e_step()
+            pipe.run(xh, ih, wh, oh)
         b_ev.record(stream)
         torch.cuda.synchronize(dev)
         e2e_s = max_over_ranks(a_ev.elapsed_time(b_ev) / 1e3, world, dev)
         if not torch.equal(oh.view(torch.int16), out.cpu().view(torch.int16)):
-            raise SystemExit("e2e output copy mismatch")
+            raise SystemExit("e2e output differs from the device-path output")
+        if ep.status_read(pipe.layout.status) != 0:
+            raise SystemExit("device status flags set during the e2e run")
+        nch = (wl.T + args.chunk_tokens - 1) // args.chunk_tokens
         e2e = {"value": aggregate_value(logical, args.e2e_steps, e2e_s, world), "unit": "GB/s",
                "ms_per_step": e2e_s * 1e3 / args.e2e_steps,
                "h2d_bytes_per_step": x.numel() * 2 + idx.numel() * 4 + w.numel() * 4,
-               "d2h_bytes_per_step": out.numel() * 2}
+               "d2h_bytes_per_step": out.numel() * 2,
+               "api": "ep_roundtrip_host (pinned host in/out, %d chunks of %d tokens)" % (
+                   nch, args.chunk_tokens)}
+        pipe.close()
+        del pipe
 
     if ep.status_read(lay.status) != 0:
         raise SystemExit("device status flags set during the timed region")
@@ -448,7 +470,8 @@ def run_ours(args, rank, world, local):
                        "logical_bytes_per_step": logical,
                        "l2": "inputs larger than L2 (x %.2f GB, dispatch buffer %.2f GB); no flush"
                              % (x.numel() * 2 / 1e9, wl.rows * wl.H * (1 if wl.payload == 'fp8' else 2) / 1e9),
-                       "parallelism": "replicas x%d" % world},
+                       "parallelism": "replicas x%d" % world,
+                       "launch": "cuda graph" if args.graph else "stream (programmatic dependent launch)"},
             "roofline": roofline,
             "kernels": kernels,
             "cpu_baseline": cpu,

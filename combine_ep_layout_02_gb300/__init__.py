@@ -6,6 +6,6 @@ combine, as hand-written CUDA kernels behind a C ABI (``include/ep.h``).
 seeded synthetic inputs.
 """
 from .binding import (  # noqa: F401
-    EpError, LayoutOut, combine, dispatch, dispatch_fp8, layout, layout_workspace_bytes, load,
-    status_read, EP_FLAG_BAD_EXPERT, EP_FLAG_OVERFLOW, EP_FLAG_BAD_ROW,
+    EpError, LayoutOut, Pipeline, combine, dispatch, dispatch_fp8, layout, layout_workspace_bytes, load,
+    layout_static_ws, status_read, EP_FLAG_BAD_EXPERT, EP_FLAG_OVERFLOW, EP_FLAG_BAD_ROW,
 )

@@ -59,6 +59,10 @@ def load():
         "ep_dispatch_fp8": ([P, i64, i64, i32, P, P, P, i64, P, P], i32),
         "ep_combine": ([P, P, P, i64, i64, i32, i64, P, P, P], i32),
         "ep_status_read": ([P, P, P], i32),
+        "ep_pipeline_create": ([i32, ctypes.POINTER(ctypes.c_void_p)], i32),
+        "ep_pipeline_destroy": ([P], i32),
+        "ep_roundtrip_host": ([P, P, P, P, P, P, i64, i64, i32, i32, i32, i32, i32, i64, P, P, P,
+                               P, i64, P, P, P, P, P, P, P, P, sz], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -206,3 +210,63 @@ def status_read(status):
     code = load().ep_status_read(_ptr(status), _stream(status.device), ctypes.byref(flags))
     _rc("ep_status_read", code)
     return int(flags.value)
+
+
+class Pipeline:
+    """Host-buffer executor (``ep_pipeline_create`` / ``ep_roundtrip_host``):
+    one layout + dispatch + combine step from pinned host inputs to a pinned
+    host output, with the copies overlapped with the kernels in token chunks.
+    Device staging buffers are allocated once here, for one workload shape."""
+
+    def __init__(self, T, H, k, E, R=1, kind="contiguous", capacity=0, chunk_tokens=4096,
+                 device=None, y=None):
+        self.T, self.H, self.k, self.E, self.R = T, H, k, E, R
+        self.kind, self.capacity, self.chunk = kind, capacity, chunk_tokens
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
+        self.rows = T * k if kind == "contiguous" else E * capacity
+        nch = max(1, (T + chunk_tokens - 1) // chunk_tokens)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            _rc("ep_pipeline_create", load().ep_pipeline_create(nch, ctypes.byref(h)))
+        self._h = h
+        self.x_dev = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.idx_dev = torch.empty(T, k, dtype=torch.int32, device=dev)
+        self.w_dev = torch.empty(T, k, dtype=torch.float32, device=dev)
+        self.out_dev = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.recv = torch.empty(self.rows, H, dtype=torch.bfloat16, device=dev)
+        self.y = y
+        self.layout = LayoutOut(torch.empty(E, dtype=torch.int32, device=dev),
+                                torch.empty(E + 1, dtype=torch.int32, device=dev),
+                                torch.empty(T, k, dtype=torch.int32, device=dev),
+                                torch.empty(R, dtype=torch.int32, device=dev),
+                                torch.zeros(1, dtype=torch.int32, device=dev))
+        self.ws = torch.empty(max(16, layout_workspace_bytes(T, k, E, R)), dtype=torch.uint8, device=dev)
+
+    def run(self, x_host, idx_host, w_host, out_host):
+        """Enqueue one step on the current stream; host tensors must be pinned."""
+        for name, t, dt in (("x_host", x_host, torch.bfloat16), ("idx_host", idx_host, torch.int32),
+                            ("w_host", w_host, torch.float32), ("out_host", out_host, torch.bfloat16)):
+            if t.is_cuda or not t.is_pinned() or t.dtype != dt or not t.is_contiguous():
+                raise ValueError("%s must be a pinned contiguous host tensor of %s" % (name, dt))
+        lay = self.layout
+        code = load().ep_roundtrip_host(
+            self._h, _stream(self.device), _ptr(x_host), _ptr(idx_host), _ptr(w_host), _ptr(out_host),
+            self.T, self.H, self.k, self.E, self.R, LAYOUT_KINDS[self.kind], self.capacity, self.chunk,
+            _ptr(self.x_dev), _ptr(self.idx_dev), _ptr(self.w_dev), _ptr(self.recv), self.rows,
+            _ptr(self.y), _ptr(self.out_dev), _ptr(lay.expert_counts), _ptr(lay.expert_offsets),
+            _ptr(lay.dst_row), _ptr(lay.rank_token_counts), _ptr(lay.status), _ptr(self.ws),
+            self.ws.numel())
+        _rc("ep_roundtrip_host", code)
+        return out_host
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().ep_pipeline_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -15,11 +15,62 @@ namespace {
 constexpr int kCombineWarps = 8;
 constexpr int kRowBatch = 8;  // rows whose loads are issued together
 
+// Accumulate one batch of up to kRowBatch rows into acc for the U column
+// groups starting at v0: all loads first, then the FMAs in j order.
+template <int U>
+__device__ __forceinline__ void accumulate_batch(const uint4* const (&src)[kRowBatch],
+                                                 const float (&wj)[kRowBatch], int64_t v0,
+                                                 int64_t nvec, int lane, float (&acc)[U][8]) {
+    uint4 buf[kRowBatch][U];
+#pragma unroll
+    for (int jj = 0; jj < kRowBatch; ++jj) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * 32 + lane;
+            buf[jj][u] = make_uint4(0, 0, 0, 0);
+            if (src[jj] != nullptr && v < nvec) buf[jj][u] = ld_stream_v4(src[jj] + v);
+        }
+    }
+#pragma unroll
+    for (int jj = 0; jj < kRowBatch; ++jj) {
+        if (src[jj] == nullptr) continue;  // warp-uniform: skipped pairs add nothing
+        const float w = wj[jj];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t wv[4] = {buf[jj][u].x, buf[jj][u].y, buf[jj][u].z, buf[jj][u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[u][2 * i] = __fmaf_rn(w, bf16lo_to_f32(wv[i]), acc[u][2 * i]);
+                acc[u][2 * i + 1] = __fmaf_rn(w, bf16hi_to_f32(wv[i]), acc[u][2 * i + 1]);
+            }
+        }
+    }
+}
+
+template <int U>
+__device__ __forceinline__ void store_bf16(uint4* out_row, int64_t v0, int64_t nvec, int lane,
+                                           const float (&acc)[U][8]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t v = v0 + u * 32 + lane;
+        if (v < nvec) {
+            uint4 o;
+            o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
+            o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
+            o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
+            o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
+            st_v4(out_row + v, o);
+        }
+    }
+}
+
 template <int U>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
                const int32_t* __restrict__ dst_row, int64_t T, int64_t nvec, int k, int64_t rows,
                uint4* __restrict__ out, uint32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     if (t >= T) return;  // warp-uniform
@@ -36,56 +87,49 @@ combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
         }
     }
     warp_flag(status, bad, EP_FLAG_BAD_ROW);
+    uint4* out_row = out + t * nvec;
 
+    if (k <= kRowBatch) {
+        // one batch: row pointers and weights stay in registers for the row
+        const uint4* src[kRowBatch];
+        float wj[kRowBatch];
+#pragma unroll
+        for (int jj = 0; jj < kRowBatch; ++jj) {
+            const int r = __shfl_sync(kFullMask, my_row, jj);
+            wj[jj] = __shfl_sync(kFullMask, my_w, jj);
+            src[jj] = (jj < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
+        }
+        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+            float acc[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+            accumulate_batch<U>(src, wj, v0, nvec, lane, acc);
+            store_bf16<U>(out_row, v0, nvec, lane, acc);
+        }
+        return;
+    }
+    // k > kRowBatch: batches of kRowBatch rows inside each column group
     for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
         float acc[U][8];
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-
         for (int j0 = 0; j0 < k; j0 += kRowBatch) {
-            uint4 buf[kRowBatch][U];
-            int rr[kRowBatch];
+            const uint4* src[kRowBatch];
+            float wj[kRowBatch];
 #pragma unroll
             for (int jj = 0; jj < kRowBatch; ++jj) {
                 const int j = j0 + jj;
-                rr[jj] = __shfl_sync(kFullMask, my_row, j & 31);
-                if (j >= k) rr[jj] = -1;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t v = v0 + u * 32 + lane;
-                    buf[jj][u] = make_uint4(0, 0, 0, 0);
-                    if (rr[jj] >= 0 && v < nvec) buf[jj][u] = ld_stream_v4(y + (int64_t)rr[jj] * nvec + v);
-                }
+                const int r = __shfl_sync(kFullMask, my_row, j & 31);
+                wj[jj] = __shfl_sync(kFullMask, my_w, j & 31);
+                src[jj] = (j < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
             }
-#pragma unroll
-            for (int jj = 0; jj < kRowBatch; ++jj) {
-                const float w = __shfl_sync(kFullMask, my_w, (j0 + jj) & 31);
-                if (rr[jj] < 0) continue;  // warp-uniform: skipped pairs add nothing
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const uint32_t wv[4] = {buf[jj][u].x, buf[jj][u].y, buf[jj][u].z, buf[jj][u].w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc[u][2 * i] = __fmaf_rn(w, bf16lo_to_f32(wv[i]), acc[u][2 * i]);
-                        acc[u][2 * i + 1] = __fmaf_rn(w, bf16hi_to_f32(wv[i]), acc[u][2 * i + 1]);
-                    }
-                }
-            }
+            accumulate_batch<U>(src, wj, v0, nvec, lane, acc);
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * 32 + lane;
-            if (v < nvec) {
-                uint4 o;
-                o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
-                o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
-                o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
-                o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
-                st_v4(out + t * nvec + v, o);
-            }
-        }
+        store_bf16<U>(out_row, v0, nvec, lane, acc);
     }
 }
 
@@ -97,10 +141,9 @@ cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* ds
     if (T == 0) return cudaSuccess;
     const int64_t nvec = H / 8;
     const unsigned grid = (unsigned)((T + kCombineWarps - 1) / kCombineWarps);
-    combine_kernel<2><<<grid, kCombineWarps * 32, 0, stream>>>(
-        static_cast<const uint4*>(y), topk_w, dst_row, T, nvec, k, rows,
-        static_cast<uint4*>(out), status);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<2>, dim3(grid), dim3(kCombineWarps * 32), 0, stream,
+                      static_cast<const uint4*>(y), topk_w, dst_row, T, nvec, k, rows,
+                      static_cast<uint4*>(out), status);
 }
 
 }  // namespace ep

@@ -10,6 +10,13 @@
 // memory (PR #1238 measures the unfused cast as a separate launch-bound step).
 #include "ep_internal.cuh"
 
+#ifndef EP_DISPATCH_BULK
+#define EP_DISPATCH_BULK 0
+#endif
+#ifndef EP_BULK_STAGES
+#define EP_BULK_STAGES 4
+#endif
+
 namespace ep {
 namespace {
 
@@ -32,31 +39,43 @@ __device__ __forceinline__ int load_dst_row(const int32_t* __restrict__ dst_row,
     return r;
 }
 
+constexpr int kRowRegs = 8;  // destination rows held in registers per pass
+
 template <int U>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k,
                      const int32_t* __restrict__ dst_row, uint4* __restrict__ recv, int64_t rows,
                      uint32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
     if (t >= T) return;  // warp-uniform
     const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const uint4* src = x + t * nvec;
-    for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
-        uint4 buf[U];
+    // k <= 8 is one pass; larger k re-reads the row once per 8 destinations
+    for (int j0 = 0; j0 < k; j0 += kRowRegs) {
+        uint4* dst[kRowRegs];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * 32 + lane;
-            if (v < nvec) buf[u] = ld_stream_v4(src + v);
+        for (int jj = 0; jj < kRowRegs; ++jj) {
+            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
+            dst[jj] = (j0 + jj < k && r >= 0) ? recv + (int64_t)r * nvec : nullptr;
         }
-        for (int j = 0; j < k; ++j) {
-            const int r = __shfl_sync(kFullMask, my_row, j);
-            if (r < 0) continue;
-            uint4* dst = recv + (int64_t)r * nvec;
+        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+            uint4 buf[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + u * 32 + lane;
-                if (v < nvec) st_v4(dst + v, buf[u]);
+                if (v < nvec) buf[u] = ld_stream_v4(src + v);
+            }
+#pragma unroll
+            for (int jj = 0; jj < kRowRegs; ++jj) {
+                if (dst[jj] == nullptr) continue;  // warp-uniform
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = v0 + u * 32 + lane;
+                    if (v < nvec) st_v4(dst[jj] + v, buf[u]);
+                }
             }
         }
     }
@@ -69,54 +88,132 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
                     const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv_q,
                     float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const int64_t nblk = H / 128;
     const uint16_t* src = x + t * H;
-    for (int64_t c0 = 0; c0 < H; c0 += 512) {
-        const int64_t c = c0 + lane * 16;
-        const bool act = c < H;  // H % 128 == 0: all 8 lanes of a block agree
-        uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-        if (act) {
-            a = ld_stream_v4(src + c);
-            b = ld_stream_v4(src + c + 8);
-        }
-        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float f[16];
+    for (int j0 = 0; j0 < k; j0 += kRowRegs) {
+        int rr[kRowRegs];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            f[2 * i] = bf16lo_to_f32(wv[i]);
-            f[2 * i + 1] = bf16hi_to_f32(wv[i]);
+        for (int jj = 0; jj < kRowRegs; ++jj) {
+            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
+            rr[jj] = (j0 + jj < k) ? r : -1;
         }
-        float amax = 0.0f;
+        for (int64_t c0 = 0; c0 < H; c0 += 512) {
+            const int64_t c = c0 + lane * 16;
+            const bool act = c < H;  // H % 128 == 0: all 8 lanes of a block agree
+            uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+            if (act) {
+                a = ld_stream_v4(src + c);
+                b = ld_stream_v4(src + c + 8);
+            }
+            const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float f[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-        const float ap = fmaxf(amax, 1e-4f);
-        const float sf = __fdiv_rn(ap, 448.0f);
-        const float inv = __fdiv_rn(448.0f, ap);
-        uint4 q;
-        uint32_t qw[4];
+            for (int i = 0; i < 8; ++i) {
+                f[2 * i] = bf16lo_to_f32(wv[i]);
+                f[2 * i + 1] = bf16hi_to_f32(wv[i]);
+            }
+            float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
-            const uint32_t hi =
-                cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
-            qw[i] = lo | (hi << 16);
-        }
-        q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-        const bool scale_writer = act && (lane & 7) == 0;
-        for (int j = 0; j < k; ++j) {
-            const int r = __shfl_sync(kFullMask, my_row, j);
-            if (r < 0) continue;
-            if (act) st_v4(recv_q + (int64_t)r * H + c, q);
-            if (scale_writer) recv_scale[(int64_t)r * nblk + (c >> 7)] = sf;
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+            const float ap = fmaxf(amax, 1e-4f);
+            const float sf = __fdiv_rn(ap, 448.0f);
+            const float inv = __fdiv_rn(448.0f, ap);
+            uint32_t qw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo =
+                    cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
+                const uint32_t hi =
+                    cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
+                qw[i] = lo | (hi << 16);
+            }
+            const uint4 q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+            const bool scale_writer = act && (lane & 7) == 0;
+#pragma unroll
+            for (int jj = 0; jj < kRowRegs; ++jj) {
+                const int r = rr[jj];
+                if (r < 0) continue;  // warp-uniform
+                if (act) st_v4(recv_q + (int64_t)r * H + c, q);
+                if (scale_writer) recv_scale[(int64_t)r * nblk + (c >> 7)] = sf;
+            }
         }
     }
+}
+
+// Bulk-copy (TMA engine) dispatch: persistent blocks of one warp; block b
+// handles tokens b, b + G, b + 2G, ...  A ring of S shared-memory stages holds
+// whole token rows: lane 0 loads a row with one cp.async.bulk completing on the
+// stage's mbarrier, then lane j (< k) writes it to destination row j with one
+// bulk store.  Loads run up to S-1 tokens ahead; a stage is refilled once the
+// stores of the token that used it have finished reading it.
+template <int S>
+__global__ void __launch_bounds__(32)
+dispatch_bf16_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, uint32_t row_bytes, int k,
+                          const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv,
+                          int64_t rows, uint32_t* __restrict__ status) {
+    extern __shared__ __align__(128) uint8_t stage_mem[];
+    __shared__ __align__(8) uint64_t bar[S];
+    const int lane = threadIdx.x;
+    const int64_t G = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t ntok = b < T ? (T - b + G - 1) / G : 0;
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    pdl_wait();
+    pdl_trigger();
+    if (ntok == 0) return;
+
+    auto load = [&](int64_t i) {  // lane 0 only
+        const int s = (int)(i % S);
+        mbar_arrive_expect_tx(&bar[s], row_bytes);
+        bulk_g2s(stage_mem + (size_t)s * row_bytes, x + (b + i * G) * (int64_t)row_bytes,
+                 row_bytes, &bar[s]);
+    };
+    if (lane == 0)
+        for (int64_t i = 0; i < S && i < ntok; ++i) load(i);
+
+    int my_row = load_dst_row(dst_row, b, k, rows, status);
+    bool timed_out = false;
+    for (int64_t i = 0; i < ntok; ++i) {
+        const int s = (int)(i % S);
+        const uint32_t parity = (uint32_t)((i / S) & 1);
+        const int next_row =
+            (i + 1 < ntok) ? load_dst_row(dst_row, b + (i + 1) * G, k, rows, status) : -1;
+        if (!mbar_wait_bounded(&bar[s], parity)) timed_out = true;
+        if (__any_sync(kFullMask, timed_out)) {
+            timed_out = true;
+            break;
+        }
+        if (lane < k) {
+            if (my_row >= 0)
+                bulk_s2g(recv + (int64_t)my_row * row_bytes, stage_mem + (size_t)s * row_bytes,
+                         row_bytes);
+            bulk_commit();  // one group per lane per token, possibly empty
+        }
+        // refill the stage of token i-1 with token i-1+S once its stores have
+        // read it (each lane's most recent group, token i, may still be pending)
+        if (i >= 1 && i - 1 + S < ntok) {
+            if (lane < k) bulk_wait_read<1>();
+            __syncwarp();
+            if (lane == 0) load(i - 1 + S);
+        }
+        my_row = next_row;
+    }
+    if (lane < k) bulk_wait_all();
+    if (timed_out && lane == 0 && status) atomicOr(status, EP_FLAG_TIMEOUT);
 }
 
 }  // namespace
@@ -125,11 +222,34 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
                                  const int32_t* dst_row, void* recv, int64_t rows,
                                  uint32_t* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
+#if EP_DISPATCH_BULK
+    {
+        constexpr int S = EP_BULK_STAGES;
+        const uint32_t row_bytes = (uint32_t)(H * 2);
+        const size_t smem = (size_t)S * row_bytes;
+        if (k <= 32 && smem <= 200 * 1024) {
+            auto kern = dispatch_bf16_bulk_kernel<S>;
+            cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            int dev = 0, sms = 0, per_sm = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem);
+            if (e != cudaSuccess) return e;
+            const int64_t want = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+            const unsigned grid = (unsigned)(T < want ? T : want);
+            return launch_pdl(kern, dim3(grid), dim3(32), smem, stream,
+                              static_cast<const uint8_t*>(x), T, row_bytes, k, dst_row,
+                              static_cast<uint8_t*>(recv), rows, status);
+        }
+    }
+#endif
     const int64_t nvec = H / 8;
     const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
-    dispatch_bf16_kernel<4><<<grid, kDispatchWarps * 32, 0, stream>>>(
-        static_cast<const uint4*>(x), T, nvec, k, dst_row, static_cast<uint4*>(recv), rows, status);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_bf16_kernel<4>, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
+                      static_cast<const uint4*>(x), T, nvec, k, dst_row, static_cast<uint4*>(recv),
+                      rows, status);
 }
 
 cudaError_t launch_dispatch_fp8(const void* x, int64_t T, int64_t H, int k,
@@ -137,9 +257,9 @@ cudaError_t launch_dispatch_fp8(const void* x, int64_t T, int64_t H, int k,
                                 int64_t rows, uint32_t* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
-    dispatch_fp8_kernel<<<grid, kDispatchWarps * 32, 0, stream>>>(
-        static_cast<const uint16_t*>(x), T, H, k, dst_row, recv_q, recv_scale, rows, status);
-    return cudaGetLastError();
+    return launch_pdl(dispatch_fp8_kernel, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
+                      static_cast<const uint16_t*>(x), T, H, k, dst_row, recv_q, recv_scale, rows,
+                      status);
 }
 
 }  // namespace ep

@@ -2,19 +2,28 @@
 // scan and stable slot assignment (the "dispatch layout" that the Prefill-like
 // profile of awsome-distributed-ai PR #1238 times inside its boundary).
 //
-// Three small kernels, no inter-block waiting:
-//   1. count  : one block per chunk of 512 tokens; a warp-aggregated
-//               (match.any) shared-memory histogram of the chunk's experts and
-//               of the tokens per virtual rank.  Written transposed,
-//               ws[column][chunk], so that phase 2 reads rows.
-//   2. scan   : one warp per column (expert or rank): exclusive scan over the
-//               chunks in place; the column total is the expert count.
+// Three small kernels chained with programmatic dependent launch; no block
+// ever waits on another block:
+//   1. count  : one 128-thread block per chunk of 128 tokens.  The chunk's
+//               ids are staged in shared memory with one coalesced pass, then
+//               shared-memory atomic histograms of experts and of tokens per
+//               virtual rank.  Written transposed, ws[column][chunk], so that
+//               phase 2 reads contiguous rows.
+//   2. scan   : one warp per column (expert or rank): each lane owns 16
+//               consecutive chunks of a 512-chunk segment (coalesced int4
+//               loads), lane sums are warp-scanned, and the exclusive prefix
+//               over chunks is written back in place.  The column total is the
+//               expert count (or the rank's token count).
 //   3. assign : one block per chunk; every block re-derives the exclusive
-//               scan over experts (E <= 1024 values), splits its chunk into 16
-//               warp sub-chunks with a shared histogram + scan, and each warp
-//               walks its pairs 32 at a time in flattened order, ranking equal
-//               experts with match.any + popc(lanemask_lt).  The slot of a
-//               pair is therefore the number of earlier pairs with the same
+//               scan over the E expert counts, splits its chunk into four
+//               32-token warp sub-chunks with a shared histogram + scan, and
+//               each warp walks its pairs 32 at a time in flattened order,
+//               ranking equal experts with popc(peers & lanemask_lt), where the
+//               peers of a lane (lanes holding the same expert) come from one
+//               ballot per bit of the expert id -- a handful of vote
+//               instructions instead of match.any, whose per-SM throughput
+//               made it the bottleneck of this kernel.  The
+//               slot of a pair is the number of earlier pairs with the same
 //               expert: a stable, deterministic assignment.
 // Masked layouts use the same slots with row = e * capacity + slot.
 #include "ep_internal.cuh"
@@ -22,77 +31,129 @@
 namespace ep {
 namespace {
 
+// Stage the chunk's pairs [p0, p0 + n) into s_idx[0 .. kLayoutTokensPerChunk*k),
+// padding the tail with kPad.
+constexpr int kPad = -2147483647 - 1;
+
+__device__ __forceinline__ void stage_ids(const int32_t* __restrict__ idx, int64_t p0, int n,
+                                          int npad, int32_t* s_idx) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(idx + p0) & 15) == 0);
+    int done = 0;
+    if (vec) {
+        const int n4 = n >> 2;
+        const int4* src = reinterpret_cast<const int4*>(idx + p0);
+        int4* dst = reinterpret_cast<int4*>(s_idx);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = __ldg(src + i);
+        done = n4 << 2;
+    }
+    for (int i = done + threadIdx.x; i < n; i += blockDim.x) s_idx[i] = __ldg(idx + p0 + i);
+    for (int i = n + threadIdx.x; i < npad; i += blockDim.x) s_idx[i] = kPad;
+}
+
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_count_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, int R_cols,
                     int64_t nchunk, int32_t* __restrict__ ws, uint32_t* __restrict__ status) {
-    extern __shared__ int32_t s_hist[];  // [E + R_cols]
+    extern __shared__ __align__(16) int32_t smem_i[];
+    const int npad = kLayoutTokensPerChunk * k;
+    int32_t* s_idx = smem_i;          // [npad]
+    int32_t* s_hist = smem_i + npad;  // [E + R_cols]
     const int ncol = E + R_cols;
+    const int64_t c = blockIdx.x;
+    const int64_t t0 = c * kLayoutTokensPerChunk;
+    const int64_t left = T - t0;
+    const int ntok = left < kLayoutTokensPerChunk ? (int)left : kLayoutTokensPerChunk;
+
+    pdl_wait();
+    pdl_trigger();
+    if (c == 0 && threadIdx.x == 0 && status) *status = 0u;
     for (int i = threadIdx.x; i < ncol; i += blockDim.x) s_hist[i] = 0;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && status) *status = 0u;
+    stage_ids(idx, t0 * k, ntok * k, npad, s_idx);
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int64_t c = blockIdx.x;
-    const int64_t tok0 = c * kLayoutTokensPerChunk + warp * 32;
-    const int64_t npairs = T * k;
-    const int64_t p0 = tok0 * k;
-
-    // experts: k pieces of 32 consecutive pairs per warp
-    for (int piece = 0; piece < k; ++piece) {
-        const int64_t p = p0 + piece * 32 + lane;
-        int e = -1;
-        if (p < npairs) e = __ldg(idx + p);
-        const bool valid = (e >= 0) && (e < E);
-        const unsigned peers = __match_any_sync(kFullMask, valid ? e : -1 - lane);
-        if (valid && (__ffs(peers) - 1) == lane) atomicAdd(&s_hist[e], __popc(peers));
+    // experts: k strided passes over the chunk's pairs
+    for (int m = 0; m < k; ++m) {
+        const int e = s_idx[m * kLayoutThreads + threadIdx.x];
+        if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
     }
-
-    // tokens per virtual rank: one token per lane, count each rank once
+    // tokens per virtual rank: one token per thread, each rank counted once
     if (R_cols > 0) {
         const int per_rank = E / R_cols;
-        const int64_t t = tok0 + lane;
-        const int32_t* row = idx + t * k;
+        const int32_t* row = s_idx + threadIdx.x * k;
+        const bool tok_ok = threadIdx.x < ntok;
         for (int j = 0; j < k; ++j) {
             int r = -1;
-            if (t < T) {
-                const int e = __ldg(row + j);
-                if (e >= 0 && e < E) {
-                    r = e / per_rank;
-                    for (int jj = 0; jj < j; ++jj) {
-                        const int e2 = __ldg(row + jj);
-                        if (e2 >= 0 && e2 < E && e2 / per_rank == r) { r = -1; break; }
-                    }
+            const int e = row[j];
+            if (tok_ok && e >= 0 && e < E) {
+                r = e / per_rank;
+                for (int jj = 0; jj < j; ++jj) {
+                    const int e2 = row[jj];
+                    if (e2 >= 0 && e2 < E && e2 / per_rank == r) { r = -1; break; }
                 }
             }
-            const unsigned peers = __match_any_sync(kFullMask, r >= 0 ? r : -1 - lane);
-            if (r >= 0 && (__ffs(peers) - 1) == lane) atomicAdd(&s_hist[E + r], __popc(peers));
+            if (r >= 0) atomicAdd(&s_hist[E + r], 1);
         }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < ncol; i += blockDim.x) ws[(int64_t)i * nchunk + c] = s_hist[i];
 }
 
-constexpr int kScanWarps = 8;
+constexpr int kScanWarps = 4;
+constexpr int kScanPerLane = 16;              // chunks per lane per segment
+constexpr int kScanSegment = 32 * kScanPerLane;
 
 __global__ void __launch_bounds__(kScanWarps * 32)
 layout_scan_kernel(int32_t* __restrict__ ws, int64_t nchunk, int E, int R_cols,
                    int32_t* __restrict__ expert_counts, int32_t* __restrict__ rank_token_counts) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int col = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
     if (col >= E + R_cols) return;
     int32_t* row = ws + (int64_t)col * nchunk;
+    // rows start 16-byte aligned only when nchunk % 4 == 0
+    const bool vec = (nchunk & 3) == 0;
     int carry = 0;
-    for (int64_t c0 = 0; c0 < nchunk; c0 += 32) {
-        const int64_t c = c0 + lane;
-        const int v = c < nchunk ? row[c] : 0;
-        int incl = v;
+    for (int64_t s0 = 0; s0 < nchunk; s0 += kScanSegment) {
+        const int64_t c0 = s0 + lane * kScanPerLane;
+        int v[kScanPerLane];
+        if (vec && c0 + kScanPerLane <= nchunk) {
+#pragma unroll
+            for (int q = 0; q < kScanPerLane / 4; ++q) {
+                const int4 a = *reinterpret_cast<const int4*>(row + c0 + 4 * q);
+                v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < kScanPerLane; ++q) v[q] = (c0 + q < nchunk) ? row[c0 + q] : 0;
+        }
+        int local = 0;
+#pragma unroll
+        for (int q = 0; q < kScanPerLane; ++q) local += v[q];
+        int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(kFullMask, incl, o);
-            if (lane >= o) incl += n;
+            const int nb = __shfl_up_sync(kFullMask, incl, o);
+            if (lane >= o) incl += nb;
         }
-        if (c < nchunk) row[c] = carry + incl - v;
+        int run = carry + incl - local;
+        if (vec && c0 + kScanPerLane <= nchunk) {
+#pragma unroll
+            for (int q = 0; q < kScanPerLane / 4; ++q) {
+                int4 a;
+                a.x = run; run += v[4 * q];
+                a.y = run; run += v[4 * q + 1];
+                a.z = run; run += v[4 * q + 2];
+                a.w = run; run += v[4 * q + 3];
+                *reinterpret_cast<int4*>(row + c0 + 4 * q) = a;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < kScanPerLane; ++q) {
+                if (c0 + q < nchunk) row[c0 + q] = run;
+                run += v[q];
+            }
+        }
         carry += __shfl_sync(kFullMask, incl, 31);
     }
     if (lane == 0) {
@@ -101,38 +162,46 @@ layout_scan_kernel(int32_t* __restrict__ ws, int64_t nchunk, int E, int R_cols,
     }
 }
 
-// Exclusive scan of counts[0..E) into s_off[0..E] by one 512-thread block.
+// Lanes of the warp whose (valid) key equals this lane's: one ballot per key
+// bit.  Invalid lanes get an empty set and appear in no valid lane's set.
+__device__ __forceinline__ unsigned warp_peers(bool valid, int key, int key_bits) {
+    unsigned peers = __ballot_sync(kFullMask, valid);
+    for (int b = 0; b < key_bits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const unsigned ones = __ballot_sync(kFullMask, bit);
+        peers &= bit ? ones : ~ones;
+    }
+    return valid ? peers : 0u;
+}
+
+// Exclusive scan of counts[0..E) into s_off[0..E] by one kLayoutThreads block.
 __device__ void block_exclusive_scan(const int32_t* __restrict__ counts, int E, int32_t* s_off,
                                      int32_t* s_warp) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    // each thread owns two consecutive experts (E <= 1024 = 2 * 512)
-    const int e0 = 2 * threadIdx.x;
-    const int a = e0 < E ? counts[e0] : 0;
-    const int b = e0 + 1 < E ? counts[e0 + 1] : 0;
-    int incl = a + b;
+    const int per = (E + kLayoutThreads - 1) / kLayoutThreads;
+    const int e0 = threadIdx.x * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+        if (e0 + i < E) local += counts[e0 + i];
+    int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(kFullMask, incl, o);
-        if (lane >= o) incl += n;
+        const int nb = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o) incl += nb;
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        int v = lane < kLayoutWarps ? s_warp[lane] : 0;
-        int w_incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(kFullMask, w_incl, o);
-            if (lane >= o) w_incl += n;
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += s_warp[w];
+    int run = wbase + incl - local;
+    for (int i = 0; i < per; ++i) {
+        if (e0 + i < E) {
+            s_off[e0 + i] = run;
+            run += counts[e0 + i];
         }
-        if (lane < kLayoutWarps) s_warp[lane] = w_incl - v;  // exclusive warp prefix
     }
-    __syncthreads();
-    const int excl = s_warp[warp] + incl - (a + b);
-    if (e0 < E) s_off[e0] = excl;
-    if (e0 + 1 < E) s_off[e0 + 1] = excl + a;
-    if (e0 + 1 == E || e0 + 2 == E) s_off[E] = excl + a + b;  // thread holding the last expert
+    if (threadIdx.x == kLayoutThreads - 1) s_off[E] = wbase + incl;
 }
 
 __global__ void __launch_bounds__(kLayoutThreads)
@@ -140,16 +209,24 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
                      int capacity, int64_t nchunk, const int32_t* __restrict__ ws,
                      const int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_offsets,
                      int32_t* __restrict__ dst_row, uint32_t* __restrict__ status) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    int32_t* s_off = reinterpret_cast<int32_t*>(smem);                  // [E + 1]
-    int32_t* s_base = s_off + (E + 1);                                  // [E]
-    int32_t* s_warp = s_base + E;                                       // [kLayoutWarps]
-    uint16_t* s_w = reinterpret_cast<uint16_t*>(s_warp + kLayoutWarps);  // [kLayoutWarps][E]
+    extern __shared__ __align__(16) int32_t smem_i[];
+    const int npad = kLayoutTokensPerChunk * k;
+    int32_t* s_idx = smem_i;                                              // [npad]
+    int32_t* s_off = s_idx + npad;                                        // [E + 1]
+    int32_t* s_base = s_off + (E + 1);                                    // [E]
+    int32_t* s_warp = s_base + E;                                         // [kLayoutWarps]
+    int32_t* s_w = s_warp + kLayoutWarps;                                 // [kLayoutWarps][E]
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t c = blockIdx.x;
+    const int64_t t0 = c * kLayoutTokensPerChunk;
+    const int64_t left = T - t0;
+    const int ntok = left < kLayoutTokensPerChunk ? (int)left : kLayoutTokensPerChunk;
 
+    pdl_wait();
+    pdl_trigger();
+    stage_ids(idx, t0 * k, ntok * k, npad, s_idx);
     block_exclusive_scan(expert_counts, E, s_off, s_warp);
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_base[e] = ws[(int64_t)e * nchunk + c];
     for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s_w[i] = 0;
@@ -157,20 +234,13 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     if (c == 0)
         for (int e = threadIdx.x; e <= E; e += blockDim.x) expert_offsets[e] = s_off[e];
 
-    const int64_t npairs = T * k;
-    const int64_t p0 = (c * kLayoutTokensPerChunk + warp * 32) * k;
-    uint16_t* my_w = s_w + warp * E;
+    const int wp0 = warp * 32 * k;  // this warp's first pair within the chunk
+    int32_t* my_w = s_w + warp * E;
 
-    // per-warp histogram of the warp's sub-chunk (each warp owns its row of
-    // s_w; within one piece distinct experts have distinct leaders)
-    for (int piece = 0; piece < k; ++piece) {
-        const int64_t p = p0 + piece * 32 + lane;
-        int e = -1;
-        if (p < npairs) e = __ldg(idx + p);
-        const bool valid = (e >= 0) && (e < E);
-        const unsigned peers = __match_any_sync(kFullMask, valid ? e : -1 - lane);
-        if (valid && (__ffs(peers) - 1) == lane) my_w[e] = (uint16_t)(my_w[e] + __popc(peers));
-        __syncwarp();
+    // per-warp histogram of the warp's 32-token sub-chunk
+    for (int m = 0; m < k; ++m) {
+        const int e = s_idx[wp0 + m * 32 + lane];
+        if (e >= 0 && e < E) atomicAdd(&my_w[e], 1);
     }
     __syncthreads();
     // exclusive scan over the warps, per expert
@@ -179,25 +249,27 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
 #pragma unroll
         for (int w = 0; w < kLayoutWarps; ++w) {
             const int v = s_w[w * E + e];
-            s_w[w * E + e] = (uint16_t)run;
+            s_w[w * E + e] = run;
             run += v;
         }
     }
     __syncthreads();
 
     const unsigned lt = lanemask_lt();
-    for (int piece = 0; piece < k; ++piece) {
-        const int64_t p = p0 + piece * 32 + lane;
-        int e = -1;
-        const bool in_range = p < npairs;
-        if (in_range) e = __ldg(idx + p);
+    const int key_bits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);  // bits that distinguish ids in [0, E)
+    const int64_t npairs = (int64_t)ntok * k;
+    int32_t* out = dst_row + t0 * k;
+    for (int m = 0; m < k; ++m) {
+        const int lp = wp0 + m * 32 + lane;   // pair within the chunk
+        const bool in_range = lp < npairs;
+        const int e = s_idx[lp];
         const bool valid = (e >= 0) && (e < E);
         const bool bad = in_range && !valid && e != -1;
-        const unsigned peers = __match_any_sync(kFullMask, valid ? e : -1 - lane);
+        const unsigned peers = warp_peers(valid, e, key_bits);
         bool overflow = false;
         int dst = -1;
         if (valid) {
-            const int slot = s_base[e] + (int)my_w[e] + __popc(peers & lt);
+            const int slot = s_base[e] + my_w[e] + __popc(peers & lt);
             if (kind == EP_LAYOUT_CONTIGUOUS) {
                 dst = s_off[e] + slot;
             } else if (slot < capacity) {
@@ -206,9 +278,9 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
                 overflow = true;
             }
         }
-        if (in_range) dst_row[p] = dst;
+        if (in_range) out[lp] = dst;
         __syncwarp();
-        if (valid && (__ffs(peers) - 1) == lane) my_w[e] = (uint16_t)(my_w[e] + __popc(peers));
+        if (valid && (__ffs(peers) - 1) == lane) my_w[e] += __popc(peers);
         __syncwarp();
         warp_flag(status, bad, EP_FLAG_BAD_EXPERT);
         warp_flag(status, overflow, EP_FLAG_OVERFLOW);
@@ -219,6 +291,8 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
 __global__ void layout_empty_kernel(int E, int R, int32_t* expert_counts,
                                     int32_t* expert_offsets, int32_t* rank_token_counts,
                                     uint32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     for (int i = threadIdx.x; i <= E; i += blockDim.x) {
         if (i < E) expert_counts[i] = 0;
         expert_offsets[i] = 0;
@@ -228,34 +302,38 @@ __global__ void layout_empty_kernel(int E, int R, int32_t* expert_counts,
     if (threadIdx.x == 0 && status) *status = 0u;
 }
 
-}  // namespace
-
-size_t layout_assign_smem_bytes(int E) {
-    return (size_t)(2 * E + 1 + kLayoutWarps) * sizeof(int32_t) +
-           (size_t)kLayoutWarps * E * sizeof(uint16_t);
+size_t count_smem_bytes(int k, int ncol) {
+    return ((size_t)kLayoutTokensPerChunk * k + ncol) * sizeof(int32_t);
 }
+
+size_t assign_smem_bytes(int k, int E) {
+    return ((size_t)kLayoutTokensPerChunk * k + 2 * E + 1 + kLayoutWarps + kLayoutWarps * E) *
+           sizeof(int32_t);
+}
+
+}  // namespace
 
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
                           int capacity, int32_t* expert_counts, int32_t* expert_offsets,
                           int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
                           int32_t* workspace, cudaStream_t stream) {
-    if (T == 0) {
-        layout_empty_kernel<<<1, 256, 0, stream>>>(E, R, expert_counts, expert_offsets,
-                                                   rank_token_counts, status);
-        return cudaGetLastError();
-    }
+    if (T == 0)
+        return launch_pdl(layout_empty_kernel, dim3(1), dim3(256), 0, stream, E, R, expert_counts,
+                          expert_offsets, rank_token_counts, status);
     const int64_t nchunk = layout_num_chunks(T);
     const int R_cols = rank_token_counts ? R : 0;
-    const size_t count_smem = (size_t)(E + R_cols) * sizeof(int32_t);
-    layout_count_kernel<<<(unsigned)nchunk, kLayoutThreads, count_smem, stream>>>(
-        topk_idx, T, k, E, R_cols, nchunk, workspace, status);
     const int ncol = E + R_cols;
-    layout_scan_kernel<<<(ncol + kScanWarps - 1) / kScanWarps, kScanWarps * 32, 0, stream>>>(
-        workspace, nchunk, E, R_cols, expert_counts, rank_token_counts);
-    layout_assign_kernel<<<(unsigned)nchunk, kLayoutThreads, layout_assign_smem_bytes(E),
-                           stream>>>(topk_idx, T, k, E, kind, capacity, nchunk, workspace,
-                                     expert_counts, expert_offsets, dst_row, status);
-    return cudaGetLastError();
+    cudaError_t err = launch_pdl(layout_count_kernel, dim3((unsigned)nchunk), dim3(kLayoutThreads),
+                                 count_smem_bytes(k, ncol), stream, topk_idx, T, k, E, R_cols,
+                                 nchunk, workspace, status);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(layout_scan_kernel, dim3((unsigned)((ncol + kScanWarps - 1) / kScanWarps)),
+                     dim3(kScanWarps * 32), 0, stream, workspace, nchunk, E, R_cols, expert_counts,
+                     rank_token_counts);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(layout_assign_kernel, dim3((unsigned)nchunk), dim3(kLayoutThreads),
+                      assign_smem_bytes(k, E), stream, topk_idx, T, k, E, kind, capacity, nchunk,
+                      workspace, expert_counts, expert_offsets, dst_row, status);
 }
 
 }  // namespace ep

@@ -69,7 +69,8 @@ typedef enum {
 enum {
     EP_FLAG_BAD_EXPERT = 1u, /* an expert id outside [-1, E): the pair was skipped */
     EP_FLAG_OVERFLOW = 2u,   /* masked layout: slot >= capacity, the pair was dropped */
-    EP_FLAG_BAD_ROW = 4u     /* dispatch/combine: dst_row outside [-1, rows): skipped */
+    EP_FLAG_BAD_ROW = 4u,    /* dispatch/combine: dst_row outside [-1, rows): skipped */
+    EP_FLAG_TIMEOUT = 8u     /* a bounded wait for an in-flight copy gave up: output incomplete */
 };
 
 typedef enum { EP_LAYOUT_CONTIGUOUS = 0, EP_LAYOUT_MASKED = 1 } ep_layout_kind_t;
@@ -134,8 +135,8 @@ EP_API int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
  * library holds until the process exits.
  *  - Returns EP_ERR_WORKSPACE, enqueueing nothing, when
  *    ep_layout_workspace_bytes(T, k, E, R, rank_token_counts != NULL) exceeds
- *    EP_STATIC_WS_BYTES.  (Example: T = 131072, E = 256, R = 32 needs 0.29 MB;
- *    the limit is about 512k int32 counters of (E+R) x ceil(T/512).)
+ *    EP_STATIC_WS_BYTES.  (Example: T = 131072, E = 256, R = 32 needs 1.18 MB;
+ *    the limit is 512k int32 counters of (E+R) x ceil(T/128).)
  *  - The first call on a device looks up the array's device address, with
  *    the caller's current device; that device must be the one `stream`
  *    belongs to.  Make the first call on each device before any stream
@@ -207,6 +208,49 @@ EP_API int ep_dispatch_fp8(const void* x, int64_t T, int64_t H, int k, const int
 EP_API int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row,
                int64_t T, int64_t H, int k, int64_t rows, void* out,
                uint32_t* status, void* stream);
+
+/*
+ * Host-buffer executor.  ep_roundtrip_host() runs one whole step -- route to
+ * the device, ep_layout, ep_dispatch, ep_combine, result back -- for inputs and
+ * output in pinned HOST memory, overlapping the copies with the kernels in
+ * token chunks: the route is copied first (the layout needs all of it), then
+ * the hidden states stream in chunk by chunk on a copy stream while earlier
+ * chunks are dispatched and combined on `stream`, and each combined chunk is
+ * copied back on a second copy stream.  (The pages time one boundary from
+ * "BF16 input and route ready" to combine completion; this call is that step
+ * seen from host memory.)
+ *
+ * A pipeline handle owns the two copy streams and the events the overlap
+ * needs; it is created once for the current device and reused.  It holds no
+ * device memory.
+ */
+EP_API int ep_pipeline_create(int max_chunks, void** handle);
+EP_API int ep_pipeline_destroy(void* handle); /* synchronises its copy streams first */
+
+/*
+ *  handle        from ep_pipeline_create on the current device;
+ *                ceil(T / chunk_tokens) <= its max_chunks.
+ *  stream        the caller's stream: when it has run past this call the
+ *                whole step, including the copy of `out_host`, is complete.
+ *  x_host        [T, H] bf16, idx_host [T, k] int32, w_host [T, k] float32,
+ *  out_host      [T, H] bf16: HOST pointers, pinned (page-locked).
+ *  x_dev, idx_dev, w_dev, out_dev   device staging buffers of the same shapes
+ *                (x_dev, out_dev 16-byte aligned).
+ *  recv, rows    the dispatch buffer, as for ep_dispatch.
+ *  y             expert outputs [rows, H] bf16 on the device, or NULL to
+ *                combine the dispatched rows themselves (identity experts).
+ *  the rest      as for ep_layout.
+ * Returns as the underlying calls do; on a non-zero return some work may
+ * already be enqueued.
+ */
+EP_API int ep_roundtrip_host(void* handle, void* stream, const void* x_host,
+                             const int32_t* idx_host, const float* w_host, void* out_host,
+                             int64_t T, int64_t H, int k, int E, int R, int kind, int capacity,
+                             int64_t chunk_tokens, void* x_dev, int32_t* idx_dev, float* w_dev,
+                             void* recv, int64_t rows, const void* y, void* out_dev,
+                             int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+                             int32_t* rank_token_counts, uint32_t* status, void* workspace,
+                             size_t workspace_bytes);
 
 /* Copy the device status word to *host_flags (a HOST pointer) after
  * synchronising `stream`. */

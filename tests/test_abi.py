@@ -51,9 +51,9 @@ def test_version_and_status_strings(lib):
 
 def test_workspace_bytes(lib):
     assert lib.ep_layout_workspace_bytes(0, 8, 256, 16, 1) == 0
-    # 65536 tokens -> 128 chunks of 512; (256 + 16) columns of int32
-    assert lib.ep_layout_workspace_bytes(65536, 8, 256, 16, 1) == 128 * 272 * 4
-    assert lib.ep_layout_workspace_bytes(65536, 8, 256, 16, 0) == 128 * 256 * 4
+    # 65536 tokens -> 512 chunks of 128; (256 + 16) columns of int32
+    assert lib.ep_layout_workspace_bytes(65536, 8, 256, 16, 1) == 512 * 272 * 4
+    assert lib.ep_layout_workspace_bytes(65536, 8, 256, 16, 0) == 512 * 256 * 4
     assert lib.ep_layout_workspace_bytes(1, 8, 3, 1, 0) == 256   # rounded up to 256 bytes
 
 
@@ -101,3 +101,12 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         binding.load()
+
+
+def test_pipeline_argument_validation(lib):
+    assert lib.ep_pipeline_create(0, ctypes.byref(ctypes.c_void_p())) == 1
+    assert lib.ep_pipeline_create(5000, ctypes.byref(ctypes.c_void_p())) == 1
+    assert lib.ep_pipeline_destroy(None) == 1
+    args = [FAKE] * 4 + [16, 64, 8, 256, 16, 0, 0, 4] + [FAKE] * 4 + [32, None, FAKE] + [FAKE] * 3 + \
+        [None, None, FAKE, 1 << 20]
+    assert lib.ep_roundtrip_host(None, None, *args) == 1     # no handle
