@@ -51,13 +51,55 @@ __device__ __forceinline__ void stage_ids(const int32_t* __restrict__ idx, int64
     for (int i = n + threadIdx.x; i < npad; i += blockDim.x) s_idx[i] = kPad;
 }
 
+// rank_of[e] = e / (E / R) for the block (one division per expert, once).
+__device__ __forceinline__ void fill_rank_table(int E, int R, int32_t* s_rank_of) {
+    const int per_rank = E / R;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_rank_of[e] = e / per_rank;
+}
+
+// Add one to s_rank_hist[r] for every virtual rank r that the token's k
+// experts (row[0..k)) reach, each rank once.  The row is read in a skewed
+// order so that the 32 lanes of a warp (32 consecutive tokens) hit distinct
+// shared-memory banks.
+__device__ __forceinline__ void count_token_ranks(const int32_t* row, int k, int E, int R,
+                                                  const int32_t* s_rank_of, int32_t* s_rank_hist) {
+    const int skew = ((threadIdx.x & 31) >> 2) % k;
+    if (R <= 64) {
+        uint64_t mask = 0;
+        for (int j = 0; j < k; ++j) {
+            int jj = j + skew;
+            if (jj >= k) jj -= k;
+            const int e = row[jj];
+            if (e >= 0 && e < E) mask |= 1ull << s_rank_of[e];
+        }
+        while (mask) {
+            const int r = __ffsll((long long)mask) - 1;
+            atomicAdd(&s_rank_hist[r], 1);
+            mask &= mask - 1;
+        }
+        return;
+    }
+    for (int j = 0; j < k; ++j) {
+        const int e = row[j];
+        if (e < 0 || e >= E) continue;
+        const int r = s_rank_of[e];
+        bool first = true;
+        for (int jj = 0; jj < j; ++jj) {
+            const int e2 = row[jj];
+            if (e2 >= 0 && e2 < E && s_rank_of[e2] == r) { first = false; break; }
+        }
+        if (first) atomicAdd(&s_rank_hist[r], 1);
+    }
+}
+
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_count_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, int R_cols,
                     int64_t nchunk, int32_t* __restrict__ ws, uint32_t* __restrict__ status) {
     extern __shared__ __align__(16) int32_t smem_i[];
     const int npad = kLayoutTokensPerChunk * k;
-    int32_t* s_idx = smem_i;          // [npad]
-    int32_t* s_hist = smem_i + npad;  // [E + R_cols]
+    int32_t* s_idx = smem_i;            // [npad]
+    int32_t* s_hist = smem_i + npad;    // [E + R_cols]
+    int32_t* s_rank_of = s_hist + E + R_cols;  // [E] when R_cols > 0
     const int ncol = E + R_cols;
     const int64_t c = blockIdx.x;
     const int64_t t0 = c * kLayoutTokensPerChunk;
@@ -68,6 +110,7 @@ layout_count_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, in
     pdl_trigger();
     if (c == 0 && threadIdx.x == 0 && status) *status = 0u;
     for (int i = threadIdx.x; i < ncol; i += blockDim.x) s_hist[i] = 0;
+    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
     stage_ids(idx, t0 * k, ntok * k, npad, s_idx);
     __syncthreads();
 
@@ -77,23 +120,8 @@ layout_count_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, in
         if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
     }
     // tokens per virtual rank: one token per thread, each rank counted once
-    if (R_cols > 0) {
-        const int per_rank = E / R_cols;
-        const int32_t* row = s_idx + threadIdx.x * k;
-        const bool tok_ok = threadIdx.x < ntok;
-        for (int j = 0; j < k; ++j) {
-            int r = -1;
-            const int e = row[j];
-            if (tok_ok && e >= 0 && e < E) {
-                r = e / per_rank;
-                for (int jj = 0; jj < j; ++jj) {
-                    const int e2 = row[jj];
-                    if (e2 >= 0 && e2 < E && e2 / per_rank == r) { r = -1; break; }
-                }
-            }
-            if (r >= 0) atomicAdd(&s_hist[E + r], 1);
-        }
-    }
+    if (R_cols > 0 && threadIdx.x < ntok)
+        count_token_ranks(s_idx + threadIdx.x * k, k, E, R_cols, s_rank_of, s_hist + E);
     __syncthreads();
     for (int i = threadIdx.x; i < ncol; i += blockDim.x) ws[(int64_t)i * nchunk + c] = s_hist[i];
 }
@@ -174,16 +202,17 @@ __device__ __forceinline__ unsigned warp_peers(bool valid, int key, int key_bits
     return valid ? peers : 0u;
 }
 
-// Exclusive scan of counts[0..E) into s_off[0..E] by one kLayoutThreads block.
-__device__ void block_exclusive_scan(const int32_t* __restrict__ counts, int E, int32_t* s_off,
-                                     int32_t* s_warp) {
+// Exclusive scan of in[0..E) (shared) into s_off[0..E] by one block of NT
+// threads; s_warp holds NT/32 ints.  Ends with the block synchronised.
+template <int NT>
+__device__ void block_exclusive_scan(const int32_t* in, int E, int32_t* s_off, int32_t* s_warp) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int per = (E + kLayoutThreads - 1) / kLayoutThreads;
+    const int per = (E + NT - 1) / NT;
     const int e0 = threadIdx.x * per;
     int local = 0;
     for (int i = 0; i < per; ++i)
-        if (e0 + i < E) local += counts[e0 + i];
+        if (e0 + i < E) local += in[e0 + i];
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -192,16 +221,26 @@ __device__ void block_exclusive_scan(const int32_t* __restrict__ counts, int E, 
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += s_warp[w];
-    int run = wbase + incl - local;
+    if (warp == 0) {
+        const int v = lane < NT / 32 ? s_warp[lane] : 0;
+        int wi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int nb = __shfl_up_sync(kFullMask, wi, o);
+            if (lane >= o) wi += nb;
+        }
+        if (lane < NT / 32) s_warp[lane] = wi - v;  // exclusive warp offsets
+        if (lane == NT / 32 - 1) s_off[E] = wi;       // grand total
+    }
+    __syncthreads();
+    int run = s_warp[warp] + incl - local;
     for (int i = 0; i < per; ++i) {
         if (e0 + i < E) {
             s_off[e0 + i] = run;
-            run += counts[e0 + i];
+            run += in[e0 + i];
         }
     }
-    if (threadIdx.x == kLayoutThreads - 1) s_off[E] = wbase + incl;
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kLayoutThreads)
@@ -214,7 +253,8 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     int32_t* s_idx = smem_i;                                              // [npad]
     int32_t* s_off = s_idx + npad;                                        // [E + 1]
     int32_t* s_base = s_off + (E + 1);                                    // [E]
-    int32_t* s_warp = s_base + E;                                         // [kLayoutWarps]
+    int32_t* s_tot = s_base + E;                                          // [E]
+    int32_t* s_warp = s_tot + E;                                          // [kLayoutWarps]
     int32_t* s_w = s_warp + kLayoutWarps;                                 // [kLayoutWarps][E]
 
     const int lane = threadIdx.x & 31;
@@ -226,11 +266,27 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
 
     pdl_wait();
     pdl_trigger();
+    // issue every global load of the prologue before the first shared store
+    constexpr int kPer = EP_MAX_EXPERTS / kLayoutThreads;
+    int cnt_v[kPer], base_v[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int e = threadIdx.x + q * kLayoutThreads;
+        cnt_v[q] = e < E ? expert_counts[e] : 0;
+        base_v[q] = e < E ? ws[(int64_t)e * nchunk + c] : 0;
+    }
     stage_ids(idx, t0 * k, ntok * k, npad, s_idx);
-    block_exclusive_scan(expert_counts, E, s_off, s_warp);
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_base[e] = ws[(int64_t)e * nchunk + c];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int e = threadIdx.x + q * kLayoutThreads;
+        if (e < E) {
+            s_tot[e] = cnt_v[q];
+            s_base[e] = base_v[q];
+        }
+    }
     for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s_w[i] = 0;
     __syncthreads();
+    block_exclusive_scan<kLayoutThreads>(s_tot, E, s_off, s_warp);
     if (c == 0)
         for (int e = threadIdx.x; e <= E; e += blockDim.x) expert_offsets[e] = s_off[e];
 
@@ -287,6 +343,103 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     }
 }
 
+// Small batches (T <= kFusedMaxTokens): the whole layout in one block of
+// 1024 threads.  Warp w owns tokens [w*tpw, (w+1)*tpw) (tpw a multiple of
+// 32); per-warp shared histograms give, after an exclusive scan over the
+// warps, each warp's base slot per expert, and the block scan over experts
+// gives the offsets -- the same stable slots as the chunked kernels, in one
+// launch.
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr int kFusedMaxTokens = 2048;
+
+__global__ void __launch_bounds__(kFusedThreads)
+layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
+                    int capacity, int tpw, int32_t* __restrict__ expert_counts,
+                    int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
+                    int32_t* __restrict__ rank_token_counts, uint32_t* __restrict__ status) {
+    extern __shared__ __align__(16) int32_t smem_i[];
+    const int npad = kFusedWarps * tpw * k;
+    int32_t* s_idx = smem_i;                    // [npad]
+    int32_t* s_w = s_idx + npad;                // [kFusedWarps][E]
+    int32_t* s_tot = s_w + kFusedWarps * E;     // [E]
+    int32_t* s_off = s_tot + E;                 // [E + 1]
+    int32_t* s_rank = s_off + E + 1;            // [R_cols]
+    int32_t* s_rank_of = s_rank + R_cols;       // [E]
+    int32_t* s_warp = s_rank_of + E;            // [kFusedWarps]
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0 && status) *status = 0u;
+    stage_ids(idx, 0, T * k, npad, s_idx);
+    for (int i = threadIdx.x; i < kFusedWarps * E; i += kFusedThreads) s_w[i] = 0;
+    for (int i = threadIdx.x; i < R_cols; i += kFusedThreads) s_rank[i] = 0;
+    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
+    __syncthreads();
+
+    const int wp0 = warp * tpw * k;
+    const int npieces = tpw * k / 32;
+    int32_t* my_w = s_w + warp * E;
+    for (int m = 0; m < npieces; ++m) {
+        const int e = s_idx[wp0 + m * 32 + lane];
+        if (e >= 0 && e < E) atomicAdd(&my_w[e], 1);
+    }
+    if (R_cols > 0)
+        for (int i = 0; i < tpw; i += 32) {
+            const int t = warp * tpw + i + lane;
+            if (t < T) count_token_ranks(s_idx + t * k, k, E, R_cols, s_rank_of, s_rank);
+        }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kFusedThreads) {
+        int run = 0;
+        for (int w = 0; w < kFusedWarps; ++w) {
+            const int v = s_w[w * E + e];
+            s_w[w * E + e] = run;
+            run += v;
+        }
+        s_tot[e] = run;
+    }
+    __syncthreads();
+    block_exclusive_scan<kFusedThreads>(s_tot, E, s_off, s_warp);
+    for (int e = threadIdx.x; e <= E; e += kFusedThreads) {
+        if (e < E) expert_counts[e] = s_tot[e];
+        expert_offsets[e] = s_off[e];
+    }
+    for (int r = threadIdx.x; r < R_cols; r += kFusedThreads) rank_token_counts[r] = s_rank[r];
+
+    const unsigned lt = lanemask_lt();
+    const int key_bits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);
+    const int npairs = T * k;
+    for (int m = 0; m < npieces; ++m) {
+        const int lp = wp0 + m * 32 + lane;
+        const bool in_range = lp < npairs;
+        const int e = s_idx[lp];
+        const bool valid = (e >= 0) && (e < E);
+        const bool bad = in_range && !valid && e != -1;
+        const unsigned peers = warp_peers(valid, e, key_bits);
+        bool overflow = false;
+        int dst = -1;
+        if (valid) {
+            const int slot = my_w[e] + __popc(peers & lt);
+            if (kind == EP_LAYOUT_CONTIGUOUS) {
+                dst = s_off[e] + slot;
+            } else if (slot < capacity) {
+                dst = e * capacity + slot;
+            } else {
+                overflow = true;
+            }
+        }
+        if (in_range) dst_row[lp] = dst;
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) my_w[e] += __popc(peers);
+        __syncwarp();
+        warp_flag(status, bad, EP_FLAG_BAD_EXPERT);
+        warp_flag(status, overflow, EP_FLAG_OVERFLOW);
+    }
+}
+
 // T == 0: write the (all-zero) outputs so that callers always get defined data.
 __global__ void layout_empty_kernel(int E, int R, int32_t* expert_counts,
                                     int32_t* expert_offsets, int32_t* rank_token_counts,
@@ -302,14 +455,22 @@ __global__ void layout_empty_kernel(int E, int R, int32_t* expert_counts,
     if (threadIdx.x == 0 && status) *status = 0u;
 }
 
-size_t count_smem_bytes(int k, int ncol) {
-    return ((size_t)kLayoutTokensPerChunk * k + ncol) * sizeof(int32_t);
+size_t count_smem_bytes(int k, int E, int R_cols) {
+    return ((size_t)kLayoutTokensPerChunk * k + E + R_cols + (R_cols > 0 ? E : 0)) * sizeof(int32_t);
 }
 
 size_t assign_smem_bytes(int k, int E) {
-    return ((size_t)kLayoutTokensPerChunk * k + 2 * E + 1 + kLayoutWarps + kLayoutWarps * E) *
+    return ((size_t)kLayoutTokensPerChunk * k + 3 * E + 1 + kLayoutWarps + kLayoutWarps * E) *
            sizeof(int32_t);
 }
+
+size_t fused_smem_bytes(int tpw, int k, int E, int R_cols) {
+    return ((size_t)kFusedWarps * tpw * k + (size_t)kFusedWarps * E + 3 * (size_t)E + 1 + R_cols +
+            kFusedWarps) *
+           sizeof(int32_t);
+}
+
+constexpr size_t kFusedSmemLimit = 160 * 1024;
 
 }  // namespace
 
@@ -320,11 +481,23 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
     if (T == 0)
         return launch_pdl(layout_empty_kernel, dim3(1), dim3(256), 0, stream, E, R, expert_counts,
                           expert_offsets, rank_token_counts, status);
-    const int64_t nchunk = layout_num_chunks(T);
     const int R_cols = rank_token_counts ? R : 0;
+    if (T <= kFusedMaxTokens) {
+        const int tpw = 32 * (int)((T + 32 * kFusedWarps - 1) / (32 * kFusedWarps));
+        const size_t smem = fused_smem_bytes(tpw, k, E, R_cols);
+        if (smem <= kFusedSmemLimit) {
+            cudaError_t err = cudaFuncSetAttribute(
+                layout_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (err != cudaSuccess) return err;
+            return launch_pdl(layout_fused_kernel, dim3(1), dim3(kFusedThreads), smem, stream,
+                              topk_idx, (int)T, k, E, R_cols, kind, capacity, tpw, expert_counts,
+                              expert_offsets, dst_row, rank_token_counts, status);
+        }
+    }
+    const int64_t nchunk = layout_num_chunks(T);
     const int ncol = E + R_cols;
     cudaError_t err = launch_pdl(layout_count_kernel, dim3((unsigned)nchunk), dim3(kLayoutThreads),
-                                 count_smem_bytes(k, ncol), stream, topk_idx, T, k, E, R_cols,
+                                 count_smem_bytes(k, E, R_cols), stream, topk_idx, T, k, E, R_cols,
                                  nchunk, workspace, status);
     if (err != cudaSuccess) return err;
     err = launch_pdl(layout_scan_kernel, dim3((unsigned)((ncol + kScanWarps - 1) / kScanWarps)),
