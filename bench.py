@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0,
                     help="scale the workload to this many tokens (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--chunk-tokens", type=int, default=4096,
+    ap.add_argument("--chunk-tokens", type=int, default=2048,
                     help="token chunk of the host-buffer executor (e2e)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the timed oracle sample (cpu_baseline)")
