@@ -54,6 +54,7 @@ def load():
         "ep_last_cuda_error": ([], i32),
         "ep_layout_workspace_bytes": ([i64, i32, i32, i32, i32], sz),
         "ep_layout": ([P, i64, i32, i32, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
+        "ep_layout_aligned": ([P, i64, i32, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "ep_layout_static_ws": ([P, i64, i32, i32, i32, i32, i32, P, P, P, P, P, P], i32),
         "ep_dispatch": ([P, i64, i64, i32, P, P, i64, P, P], i32),
         "ep_dispatch_fp8": ([P, i64, i64, i32, P, P, P, i64, P, P], i32),
@@ -103,9 +104,15 @@ def layout_workspace_bytes(T, k, E, R, with_rank_counts=True):
     return int(load().ep_layout_workspace_bytes(T, k, E, R, 1 if with_rank_counts else 0))
 
 
+def aligned_rows_bound(T, k, E, alignment):
+    """Rows a dispatch buffer needs for any route under ``ep_layout_aligned``."""
+    return T * k + E * (alignment - 1)
+
+
 def layout(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=None, workspace=None,
-           with_rank_counts=True):
-    """Routing layout of ``topk_idx`` [T, k] int32 (see ``ep_layout``)."""
+           with_rank_counts=True, alignment=1):
+    """Routing layout of ``topk_idx`` [T, k] int32 (see ``ep_layout``; with
+    ``alignment`` > 1, ``ep_layout_aligned``, contiguous only)."""
     _check_dev("topk_idx", topk_idx, torch.int32)
     T, k = topk_idx.shape
     dev = topk_idx.device
@@ -121,6 +128,15 @@ def layout(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=None, workspa
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if alignment != 1:
+        if kind != "contiguous":
+            raise ValueError("expert alignment applies to the contiguous layout only")
+        code = load().ep_layout_aligned(_ptr(topk_idx), T, k, E, R, alignment,
+                                        _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                        _ptr(out.dst_row), _ptr(out.rank_token_counts),
+                                        _ptr(out.status), _ptr(workspace), wbytes, _stream(dev))
+        _rc("ep_layout_aligned", code)
+        return out
     code = load().ep_layout(_ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity,
                             _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.dst_row),
                             _ptr(out.rank_token_counts), _ptr(out.status), _ptr(workspace), wbytes,

@@ -58,16 +58,21 @@ size_t ep_layout_workspace_bytes(int64_t T, int k, int E, int R, int with_rank_c
     return (bytes + 255) & ~(size_t)255;
 }
 
-int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind, int capacity,
-              int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
-              int32_t* rank_token_counts, uint32_t* status, void* workspace,
-              size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int layout_checked(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind, int capacity,
+                   int align, int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+                   int32_t* rank_token_counts, uint32_t* status, void* workspace,
+                   size_t workspace_bytes, void* stream) {
     if (T < 0 || k < 1 || k > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || E % R != 0)
         return EP_ERR_INVALID_ARG;
     if (T > (int64_t)INT32_MAX / k) return EP_ERR_INVALID_ARG;
     if (kind != EP_LAYOUT_CONTIGUOUS && kind != EP_LAYOUT_MASKED) return EP_ERR_INVALID_ARG;
     if (kind == EP_LAYOUT_MASKED && (capacity < 0 || (int64_t)E * capacity > (int64_t)INT32_MAX))
         return EP_ERR_INVALID_ARG;
+    if (align < 1 || T * k + (int64_t)E * (align - 1) > (int64_t)INT32_MAX) return EP_ERR_INVALID_ARG;
     if (!expert_counts || !expert_offsets) return EP_ERR_INVALID_ARG;
     if (T > 0 && (!topk_idx || !dst_row)) return EP_ERR_INVALID_ARG;
     if (!aligned(topk_idx, 4) || !aligned(dst_row, 4) || !aligned(expert_counts, 4) ||
@@ -78,9 +83,31 @@ int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
         if (!workspace || workspace_bytes < need) return EP_ERR_WORKSPACE;
         if (!aligned(workspace, 16)) return EP_ERR_ALIGNMENT;
     }
-    return cuda_status(ep::launch_layout(topk_idx, T, k, E, R, kind, capacity, expert_counts,
-                                         expert_offsets, dst_row, rank_token_counts, status,
-                                         static_cast<int32_t*>(workspace), as_stream(stream)));
+    return cuda_status(ep::launch_layout(topk_idx, T, k, E, R, kind, capacity, align,
+                                         expert_counts, expert_offsets, dst_row, rank_token_counts,
+                                         status, static_cast<int32_t*>(workspace),
+                                         as_stream(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind, int capacity,
+              int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+              int32_t* rank_token_counts, uint32_t* status, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    return layout_checked(topk_idx, T, k, E, R, kind, capacity, 1, expert_counts, expert_offsets,
+                          dst_row, rank_token_counts, status, workspace, workspace_bytes, stream);
+}
+
+int ep_layout_aligned(const int32_t* topk_idx, int64_t T, int k, int E, int R, int alignment,
+                      int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+                      int32_t* rank_token_counts, uint32_t* status, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    return layout_checked(topk_idx, T, k, E, R, EP_LAYOUT_CONTIGUOUS, 0, alignment, expert_counts,
+                          expert_offsets, dst_row, rank_token_counts, status, workspace,
+                          workspace_bytes, stream);
 }
 
 int ep_dispatch(const void* x, int64_t T, int64_t H, int k, const int32_t* dst_row, void* recv,

@@ -12,7 +12,14 @@
 namespace ep {
 namespace {
 
-constexpr int kCombineWarps = 8;
+#ifndef EP_COMBINE_U
+#define EP_COMBINE_U 2  // column groups (16-byte vectors per lane) per pass
+#endif
+#ifndef EP_COMBINE_WARPS
+#define EP_COMBINE_WARPS 4
+#endif
+
+constexpr int kCombineWarps = EP_COMBINE_WARPS;
 constexpr int kRowBatch = 8;  // rows whose loads are issued together
 
 // Accumulate one batch of up to kRowBatch rows into acc for the U column
@@ -141,7 +148,7 @@ cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* ds
     if (T == 0) return cudaSuccess;
     const int64_t nvec = H / 8;
     const unsigned grid = (unsigned)((T + kCombineWarps - 1) / kCombineWarps);
-    return launch_pdl(combine_kernel<2>, dim3(grid), dim3(kCombineWarps * 32), 0, stream,
+    return launch_pdl(combine_kernel<EP_COMBINE_U>, dim3(grid), dim3(kCombineWarps * 32), 0, stream,
                       static_cast<const uint4*>(y), topk_w, dst_row, T, nvec, k, rows,
                       static_cast<uint4*>(out), status);
 }

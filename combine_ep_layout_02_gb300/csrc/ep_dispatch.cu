@@ -16,6 +16,12 @@
 #ifndef EP_BULK_STAGES
 #define EP_BULK_STAGES 4
 #endif
+#ifndef EP_DISPATCH_U
+#define EP_DISPATCH_U 4  // 16-byte vectors per lane in flight per row pass
+#endif
+#ifndef EP_DISPATCH_STORE_CS
+#define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
+#endif
 
 namespace ep {
 namespace {
@@ -74,7 +80,10 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t v = v0 + u * 32 + lane;
-                    if (v < nvec) st_v4(dst[jj] + v, buf[u]);
+                    if (v < nvec) {
+                        if (EP_DISPATCH_STORE_CS) st_cs_v4(dst[jj] + v, buf[u]);
+                        else st_v4(dst[jj] + v, buf[u]);
+                    }
                 }
             }
         }
@@ -247,7 +256,7 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
 #endif
     const int64_t nvec = H / 8;
     const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
-    return launch_pdl(dispatch_bf16_kernel<4>, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
+    return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U>, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
                       static_cast<const uint4*>(x), T, nvec, k, dst_row, static_cast<uint4*>(recv),
                       rows, status);
 }

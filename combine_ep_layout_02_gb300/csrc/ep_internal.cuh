@@ -199,7 +199,7 @@ inline int64_t layout_num_chunks(int64_t T) {
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
-                          int capacity, int32_t* expert_counts, int32_t* expert_offsets,
+                          int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
                           int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
                           int32_t* workspace, cudaStream_t stream);
 

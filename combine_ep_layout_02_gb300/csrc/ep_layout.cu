@@ -25,7 +25,9 @@
 //               made it the bottleneck of this kernel.  The
 //               slot of a pair is the number of earlier pairs with the same
 //               expert: a stable, deterministic assignment.
-// Masked layouts use the same slots with row = e * capacity + slot.
+// Masked layouts use the same slots with row = e * capacity + slot.  With an
+// expert alignment m > 1 (contiguous only) each expert's segment is padded to
+// a multiple of m rows: the offsets scan ceil(count / m) * m instead.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -245,7 +247,7 @@ __device__ void block_exclusive_scan(const int32_t* in, int E, int32_t* s_off, i
 
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, int kind,
-                     int capacity, int64_t nchunk, const int32_t* __restrict__ ws,
+                     int capacity, int align, int64_t nchunk, const int32_t* __restrict__ ws,
                      const int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_offsets,
                      int32_t* __restrict__ dst_row, uint32_t* __restrict__ status) {
     extern __shared__ __align__(16) int32_t smem_i[];
@@ -280,7 +282,7 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     for (int q = 0; q < kPer; ++q) {
         const int e = threadIdx.x + q * kLayoutThreads;
         if (e < E) {
-            s_tot[e] = cnt_v[q];
+            s_tot[e] = (cnt_v[q] + align - 1) / align * align;  // padded segment length
             s_base[e] = base_v[q];
         }
     }
@@ -355,7 +357,7 @@ constexpr int kFusedMaxTokens = 2048;
 
 __global__ void __launch_bounds__(kFusedThreads)
 layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
-                    int capacity, int tpw, int32_t* __restrict__ expert_counts,
+                    int capacity, int align, int tpw, int32_t* __restrict__ expert_counts,
                     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
                     int32_t* __restrict__ rank_token_counts, uint32_t* __restrict__ status) {
     extern __shared__ __align__(16) int32_t smem_i[];
@@ -399,14 +401,12 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
             s_w[w * E + e] = run;
             run += v;
         }
-        s_tot[e] = run;
+        expert_counts[e] = run;
+        s_tot[e] = (run + align - 1) / align * align;  // padded segment length
     }
     __syncthreads();
     block_exclusive_scan<kFusedThreads>(s_tot, E, s_off, s_warp);
-    for (int e = threadIdx.x; e <= E; e += kFusedThreads) {
-        if (e < E) expert_counts[e] = s_tot[e];
-        expert_offsets[e] = s_off[e];
-    }
+    for (int e = threadIdx.x; e <= E; e += kFusedThreads) expert_offsets[e] = s_off[e];
     for (int r = threadIdx.x; r < R_cols; r += kFusedThreads) rank_token_counts[r] = s_rank[r];
 
     const unsigned lt = lanemask_lt();
@@ -475,7 +475,7 @@ constexpr size_t kFusedSmemLimit = 160 * 1024;
 }  // namespace
 
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
-                          int capacity, int32_t* expert_counts, int32_t* expert_offsets,
+                          int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
                           int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
                           int32_t* workspace, cudaStream_t stream) {
     if (T == 0)
@@ -490,7 +490,8 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                 layout_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (err != cudaSuccess) return err;
             return launch_pdl(layout_fused_kernel, dim3(1), dim3(kFusedThreads), smem, stream,
-                              topk_idx, (int)T, k, E, R_cols, kind, capacity, tpw, expert_counts,
+                              topk_idx, (int)T, k, E, R_cols, kind, capacity, align, tpw,
+                              expert_counts,
                               expert_offsets, dst_row, rank_token_counts, status);
         }
     }
@@ -505,7 +506,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                      rank_token_counts);
     if (err != cudaSuccess) return err;
     return launch_pdl(layout_assign_kernel, dim3((unsigned)nchunk), dim3(kLayoutThreads),
-                      assign_smem_bytes(k, E), stream, topk_idx, T, k, E, kind, capacity, nchunk,
+                      assign_smem_bytes(k, E), stream, topk_idx, T, k, E, kind, capacity, align, nchunk,
                       workspace, expert_counts, expert_offsets, dst_row, status);
 }
 

@@ -109,6 +109,9 @@ EP_API size_t ep_layout_workspace_bytes(int64_t T, int k, int E, int R, int with
  *                    EP_FLAG_BAD_EXPERT.
  *  rank_token_counts [R] int32 out or NULL: tokens with at least one valid
  *                    expert in virtual rank r.
+ *                    The layout may be computed once and reused by any number
+ *                    of ep_dispatch / ep_combine calls for the same route
+ *                    (the pages' "cached dispatch").
  *  status            [1] uint32 or NULL: zeroed, then device flags OR-ed in.
  *  workspace         device scratch of at least
  *                    ep_layout_workspace_bytes(T, k, E, R, rank_token_counts != NULL)
@@ -121,6 +124,23 @@ EP_API int ep_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
               int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
               int32_t* rank_token_counts, uint32_t* status,
               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * ep_layout_aligned -- the contiguous layout for a grouped-GEMM consumer that
+ * wants every expert's rows to start on a multiple of `alignment` rows (the
+ * "expert_alignment" setting of the DeepEP dispatch mode that PR #1238's
+ * kernel-level re-run pins to 1).  Expert e's segment is
+ * ceil(expert_counts[e] / alignment) * alignment rows long, so
+ * expert_offsets[e] is a multiple of `alignment`; slots are those of
+ * ep_layout.  The padding rows receive no pair: dispatch leaves them untouched
+ * and combine never reads them.  The buffer needs expert_offsets[E] rows, at
+ * most T*k + E*(alignment-1).  alignment == 1 is ep_layout(..contiguous..).
+ * Requires alignment >= 1 and T*k + E*(alignment-1) < 2^31.
+ */
+EP_API int ep_layout_aligned(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                             int alignment, int32_t* expert_counts, int32_t* expert_offsets,
+                             int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * ep_layout_static_ws -- ep_layout() for callers that cannot allocate device

@@ -42,6 +42,8 @@ def _load():
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_layout.argtypes = [P, i64, i32, i32, i32, i32, i32, P, P, P, P]
         lib.oracle_layout.restype = ctypes.c_uint32
+        lib.oracle_layout_aligned.argtypes = [P, i64, i32, i32, i32, i32, P, P, P, P]
+        lib.oracle_layout_aligned.restype = ctypes.c_uint32
         lib.oracle_dispatch_bf16.argtypes = [P, i64, i64, i32, P, P]
         lib.oracle_dispatch_bf16.restype = None
         lib.oracle_quantize_row_fp8.argtypes = [P, i64, P, P]
@@ -101,6 +103,22 @@ def layout(topk_idx, E, R=1, kind=LAYOUT_CONTIGUOUS, capacity=0):
         raise ValueError("oracle_layout: invalid sizes")
     return dict(counts=counts, offsets=offsets, dst_row=dst,
                 rank_token_counts=rtc, flags=int(flags))
+
+
+def layout_aligned(topk_idx, E, R=1, alignment=1):
+    """Contiguous layout with expert segments padded to multiples of `alignment`."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    dst = np.zeros((T, k), np.int32)
+    rtc = np.zeros(R, np.int32)
+    flags = _load().oracle_layout_aligned(_p(idx), T, k, E, R, alignment, _p(counts), _p(offsets),
+                                          _p(dst), _p(rtc))
+    if flags == 0xFFFFFFFF:
+        raise ValueError("oracle_layout_aligned: invalid sizes")
+    return dict(counts=counts, offsets=offsets, dst_row=dst, rank_token_counts=rtc,
+                flags=int(flags))
 
 
 # --- dispatch -------------------------------------------------------------
@@ -177,6 +195,6 @@ def library_path():
 __all__ = [
     "LAYOUT_CONTIGUOUS", "LAYOUT_MASKED", "FLAG_BAD_EXPERT", "FLAG_OVERFLOW",
     "bf16_to_float", "bf16_from_double", "e4m3_decode", "e4m3_encode",
-    "layout", "dispatch_bf16", "quantize_row_fp8", "dispatch_fp8",
+    "layout", "layout_aligned", "dispatch_bf16", "quantize_row_fp8", "dispatch_fp8",
     "combine_f64", "combine_fp32_seq", "library_path",
 ]

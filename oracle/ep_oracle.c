@@ -176,6 +176,33 @@ uint32_t oracle_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
     return flags;
 }
 
+/* The same layout for a grouped-GEMM consumer that wants every expert's rows
+ * to start on a multiple of `alignment` (the "expert_alignment" setting that
+ * PR #1238's kernel-level re-run pins to 1): the segment of expert e is
+ * ceil(count_e / alignment) * alignment rows long; padding rows receive no
+ * pair.  The slots are those of oracle_layout; only the segment starts move. */
+uint32_t oracle_layout_aligned(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                               int alignment, int32_t* counts, int32_t* offsets,
+                               int32_t* dst_row, int32_t* rank_token_counts) {
+    if (alignment < 1) return 0xFFFFFFFFu;
+    uint32_t flags = oracle_layout(topk_idx, T, k, E, R, ORACLE_LAYOUT_CONTIGUOUS, 0, counts,
+                                   offsets, dst_row, rank_token_counts);
+    if (flags == 0xFFFFFFFFu) return flags;
+    int64_t npairs = T * (int64_t)k;
+    /* slot of each pair = its packed row minus the packed offset of its expert */
+    int64_t run = 0;
+    for (int e = 0; e < E; ++e) {
+        int64_t padded = ((int64_t)counts[e] + alignment - 1) / alignment * alignment;
+        int32_t packed = offsets[e];
+        for (int64_t p = 0; p < npairs; ++p)
+            if (dst_row[p] >= 0 && topk_idx[p] == e) dst_row[p] = (int32_t)(run + (dst_row[p] - packed));
+        offsets[e] = (int32_t)run;
+        run += padded;
+    }
+    offsets[E] = (int32_t)run;
+    return flags;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Dispatch                                                                 */
 /* ------------------------------------------------------------------------ */

@@ -40,6 +40,14 @@ uint32_t oracle_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
                        int32_t* offsets, int32_t* dst_row,
                        int32_t* rank_token_counts);
 
+/* Routing layout with each expert's contiguous segment padded to a multiple
+ * of `alignment` rows: offsets are the exclusive scan of
+ * ceil(count / alignment) * alignment.  Contiguous kind only; alignment 1 is
+ * oracle_layout(). */
+uint32_t oracle_layout_aligned(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                               int alignment, int32_t* counts, int32_t* offsets,
+                               int32_t* dst_row, int32_t* rank_token_counts);
+
 /* BF16 dispatch: recv[dst_row[t,j], :] = x[t, :] for every pair with
  * dst_row >= 0.  x is [T,H], recv is [rows,H], both bf16 bit patterns. */
 void oracle_dispatch_bf16(const uint16_t* x, int64_t T, int64_t H, int k,

@@ -110,3 +110,14 @@ def test_pipeline_argument_validation(lib):
     args = [FAKE] * 4 + [16, 64, 8, 256, 16, 0, 0, 4] + [FAKE] * 4 + [32, None, FAKE] + [FAKE] * 3 + \
         [None, None, FAKE, 1 << 20]
     assert lib.ep_roundtrip_host(None, None, *args) == 1     # no handle
+
+
+def test_aligned_layout_argument_validation(lib):
+    def call(T=16, k=8, E=256, R=16, align=8, ws=FAKE):
+        return lib.ep_layout_aligned(FAKE, T, k, E, R, align, FAKE, FAKE, FAKE, None, None, ws,
+                                     1 << 30, None)
+    assert call(align=0) == 1
+    assert call(align=-3) == 1
+    assert call(T=1 << 27, k=8, E=1024, R=1, align=1 << 21) == 1   # padded rows >= 2^31
+    assert call(E=255) == 1
+    assert call(ws=None) == 3

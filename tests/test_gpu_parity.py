@@ -326,3 +326,49 @@ def test_combine_full_size_fp8_workload_sampled():
     got = _bits(out[torch.from_numpy(ts).to(DEV)])
     check_combine(got, ref, absum, "prefill_fp8 full")
     assert np.array_equal(got, oracle.combine_fp32_seq(yb, wb, compact))
+
+
+# --------------------------------------------------------------------------- expert alignment, reuse
+
+@pytest.mark.parametrize("T,k,E,R,alignment", [(1, 1, 1, 1, 4), (700, 8, 256, 16, 128), (3000, 8, 64, 4, 8),
+                                               (2048, 4, 128, 4, 16), (129, 3, 7, 7, 2)])
+def test_aligned_layout_and_path(T, k, E, R, alignment):
+    rng = np.random.default_rng(T + alignment)
+    idx = rng.integers(-1, E, size=(T, k)).astype(np.int32)
+    lay = ep.layout(torch.from_numpy(idx).to(DEV), E, R, "contiguous", alignment=alignment)
+    ref = oracle.layout_aligned(idx, E, R, alignment)
+    assert np.array_equal(lay.expert_counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(lay.expert_offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(lay.dst_row.cpu().numpy(), ref["dst_row"])
+    assert np.array_equal(lay.rank_token_counts.cpu().numpy(), ref["rank_token_counts"])
+    assert ep.status_read(lay.status) == ref["flags"]
+    rows = ep.binding.aligned_rows_bound(T, k, E, alignment)
+    assert int(lay.expert_offsets[-1]) <= rows
+    H = 256
+    x = torch.randn(T, H, device=DEV).to(torch.bfloat16)
+    recv = torch.full((rows, H), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    ep.dispatch(x, lay.dst_row, rows, recv=recv)
+    rrecv = oracle.dispatch_bf16(_bits(x), ref["dst_row"], rows,
+                                 recv=np.full((rows, H), np.uint16(0xABCD), np.uint16))
+    assert np.array_equal(_bits(recv), rrecv)          # padding rows keep the sentinel
+    w = torch.rand(T, k, device=DEV)
+    out = ep.combine(recv, w, lay.dst_row)
+    assert np.array_equal(_bits(out), oracle.combine_fp32_seq(rrecv, w.cpu().numpy(), ref["dst_row"]))
+
+
+def test_layout_reused_across_calls():
+    # the route is fixed: one layout serves several dispatch / combine calls
+    wl = W.WORKLOADS["masked"].scaled(T=900, H=512, capacity=900)
+    idx = W.route(wl, device=DEV)
+    lay = ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity)
+    ref = oracle.layout(idx.cpu().numpy(), wl.E, wl.R, oracle.LAYOUT_MASKED, wl.capacity)
+    for seed in range(3):
+        g = torch.Generator(device=DEV).manual_seed(seed)
+        x = torch.randn(wl.T, wl.H, generator=g, device=DEV).to(torch.bfloat16)
+        w = torch.rand(wl.T, wl.k, generator=g, device=DEV)
+        recv = ep.dispatch(x, lay.dst_row, wl.rows)
+        out = ep.combine(recv, w, lay.dst_row)
+        rrecv = oracle.dispatch_bf16(_bits(x), ref["dst_row"], wl.rows)
+        used = rows_of(ref["dst_row"])
+        assert np.array_equal(_bits(recv)[used], rrecv[used])
+        assert np.array_equal(_bits(out), oracle.combine_fp32_seq(rrecv, w.cpu().numpy(), ref["dst_row"]))

@@ -157,3 +157,28 @@ def test_logical_bytes_match_published_payload():
         # the printed per-rank payload is one dispatch plus one combine
         assert round((disp + comb) / 1e6, 2) == case["MB_per_rank"]
         assert disp + comb == case["bytes"]
+
+
+@pytest.mark.parametrize("alignment", [1, 2, 8, 128])
+@pytest.mark.parametrize("T,k,E", [(1, 1, 1), (40, 8, 16), (300, 4, 7)])
+def test_aligned_layout_matches_brute_force(T, k, E, alignment):
+    rng = np.random.default_rng(T + k * 17 + E * 101 + alignment)
+    idx = rng.integers(-1, E, size=(T, k)).astype(np.int32)
+    got = oracle.layout_aligned(idx, E, 1, alignment)
+    counts, _, _, _, flags = brute_force_layout(idx, E, 1, oracle.LAYOUT_CONTIGUOUS, 0)
+    # segment starts: running sum of counts rounded up to the alignment
+    starts = [0]
+    for e in range(E):
+        starts.append(starts[-1] + -(-int(counts[e]) // alignment) * alignment)
+    assert got["offsets"].tolist() == starts
+    assert all(o % alignment == 0 for o in starts)
+    flat = idx.reshape(-1)
+    dst = got["dst_row"].reshape(-1)
+    for p, e in enumerate(flat):
+        if 0 <= e < E:
+            slot = sum(1 for q in range(p) if flat[q] == e)
+            assert dst[p] == starts[e] + slot
+        else:
+            assert dst[p] == -1
+    assert got["flags"] == flags
+    assert np.array_equal(got["counts"], counts)
