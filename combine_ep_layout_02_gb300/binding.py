@@ -63,7 +63,7 @@ def load():
         "ep_pipeline_create": ([i32, ctypes.POINTER(ctypes.c_void_p)], i32),
         "ep_pipeline_destroy": ([P], i32),
         "ep_roundtrip_host": ([P, P, P, P, P, P, i64, i64, i32, i32, i32, i32, i32, i64, P, P, P,
-                               P, i64, P, P, P, P, P, P, P, P, sz], i32),
+                               P, P, P, i64, P, P, P, P, P, P, P, P, sz], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -234,8 +234,8 @@ class Pipeline:
     host output, with the copies overlapped with the kernels in token chunks.
     Device staging buffers are allocated once here, for one workload shape."""
 
-    def __init__(self, T, H, k, E, R=1, kind="contiguous", capacity=0, chunk_tokens=4096,
-                 device=None, y=None):
+    def __init__(self, T, H, k, E, R=1, kind="contiguous", capacity=0, chunk_tokens=2048,
+                 device=None, y=None, payload="bf16"):
         self.T, self.H, self.k, self.E, self.R = T, H, k, E, R
         self.kind, self.capacity, self.chunk = kind, capacity, chunk_tokens
         dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
@@ -250,7 +250,16 @@ class Pipeline:
         self.idx_dev = torch.empty(T, k, dtype=torch.int32, device=dev)
         self.w_dev = torch.empty(T, k, dtype=torch.float32, device=dev)
         self.out_dev = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-        self.recv = torch.empty(self.rows, H, dtype=torch.bfloat16, device=dev)
+        self.payload = payload
+        if payload == "fp8":
+            if y is None:
+                raise ValueError("FP8 dispatch needs the expert outputs y to combine")
+            self.recv = None
+            self.recv_q = torch.empty(self.rows, H, dtype=torch.uint8, device=dev)
+            self.recv_scale = torch.empty(self.rows, H // 128, dtype=torch.float32, device=dev)
+        else:
+            self.recv = torch.empty(self.rows, H, dtype=torch.bfloat16, device=dev)
+            self.recv_q = self.recv_scale = None
         self.y = y
         self.layout = LayoutOut(torch.empty(E, dtype=torch.int32, device=dev),
                                 torch.empty(E + 1, dtype=torch.int32, device=dev),
@@ -269,7 +278,8 @@ class Pipeline:
         code = load().ep_roundtrip_host(
             self._h, _stream(self.device), _ptr(x_host), _ptr(idx_host), _ptr(w_host), _ptr(out_host),
             self.T, self.H, self.k, self.E, self.R, LAYOUT_KINDS[self.kind], self.capacity, self.chunk,
-            _ptr(self.x_dev), _ptr(self.idx_dev), _ptr(self.w_dev), _ptr(self.recv), self.rows,
+            _ptr(self.x_dev), _ptr(self.idx_dev), _ptr(self.w_dev), _ptr(self.recv),
+            _ptr(self.recv_q), _ptr(self.recv_scale), self.rows,
             _ptr(self.y), _ptr(self.out_dev), _ptr(lay.expert_counts), _ptr(lay.expert_offsets),
             _ptr(lay.dst_row), _ptr(lay.rank_token_counts), _ptr(lay.status), _ptr(self.ws),
             self.ws.numel())

@@ -90,7 +90,8 @@ int ep_pipeline_destroy(void* handle) {
 int ep_roundtrip_host(void* handle, void* stream, const void* x_host, const int32_t* idx_host,
                       const float* w_host, void* out_host, int64_t T, int64_t H, int k, int E,
                       int R, int kind, int capacity, int64_t chunk_tokens, void* x_dev,
-                      int32_t* idx_dev, float* w_dev, void* recv, int64_t rows, const void* y,
+                      int32_t* idx_dev, float* w_dev, void* recv, uint8_t* recv_q,
+                      float* recv_scale, int64_t rows, const void* y,
                       void* out_dev, int32_t* expert_counts, int32_t* expert_offsets,
                       int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
                       void* workspace, size_t workspace_bytes) {
@@ -101,10 +102,15 @@ int ep_roundtrip_host(void* handle, void* stream, const void* x_host, const int3
     if (H % 8 != 0) return EP_ERR_ALIGNMENT;
     const int64_t nchunks = T > 0 ? (T + chunk_tokens - 1) / chunk_tokens : 0;
     if (nchunks > p->max_chunks) return EP_ERR_INVALID_ARG;
+    const bool fp8 = recv_q != nullptr;
     if (T > 0 && (!x_host || !idx_host || !w_host || !out_host || !x_dev || !idx_dev || !w_dev ||
-                  !out_dev || (!recv && rows > 0)))
+                  !out_dev))
         return EP_ERR_INVALID_ARG;
-    if (!aligned16(x_dev) || !aligned16(out_dev) || !aligned16(recv) || !aligned16(y))
+    // FP8 dispatch needs its scale buffer and expert outputs to combine;
+    // BF16 dispatch needs its buffer (combined directly when y is NULL)
+    if (fp8 ? (!recv_scale || !y) : (!recv && rows > 0)) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x_dev) || !aligned16(out_dev) || !aligned16(recv) || !aligned16(y) ||
+        !aligned16(recv_q))
         return EP_ERR_ALIGNMENT;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) return EP_ERR_INVALID_ARG;
@@ -154,8 +160,10 @@ int ep_roundtrip_host(void* handle, void* stream, const void* x_host, const int3
         const int64_t t0 = c * chunk_tokens;
         const int64_t tn = (T - t0 < chunk_tokens) ? T - t0 : chunk_tokens;
         if ((e = cudaStreamWaitEvent(cs, p->x_ready[c], 0)) != cudaSuccess) return fail(e);
-        rc = ep_dispatch(static_cast<const char*>(x_dev) + t0 * xrow, tn, H, k, dst_row + t0 * k,
-                         recv, rows, status, stream);
+        rc = fp8 ? ep_dispatch_fp8(static_cast<const char*>(x_dev) + t0 * xrow, tn, H, k,
+                                   dst_row + t0 * k, recv_q, recv_scale, rows, status, stream)
+                 : ep_dispatch(static_cast<const char*>(x_dev) + t0 * xrow, tn, H, k,
+                               dst_row + t0 * k, recv, rows, status, stream);
         if (rc != EP_OK) return rc;
         rc = ep_combine(ysrc, w_dev + t0 * k, dst_row + t0 * k, tn, H, k, rows,
                         static_cast<char*>(out_dev) + t0 * xrow, status, stream);

@@ -256,9 +256,12 @@ EP_API int ep_pipeline_destroy(void* handle); /* synchronises its copy streams f
  *  out_host      [T, H] bf16: HOST pointers, pinned (page-locked).
  *  x_dev, idx_dev, w_dev, out_dev   device staging buffers of the same shapes
  *                (x_dev, out_dev 16-byte aligned).
- *  recv, rows    the dispatch buffer, as for ep_dispatch.
- *  y             expert outputs [rows, H] bf16 on the device, or NULL to
- *                combine the dispatched rows themselves (identity experts).
+ *  recv, rows    the BF16 dispatch buffer, as for ep_dispatch; or, when
+ *  recv_q        is not NULL, FP8 dispatch into recv_q / recv_scale as for
+ *                ep_dispatch_fp8 (recv may then be NULL).
+ *  y             expert outputs [rows, H] bf16 on the device, or NULL (BF16
+ *                dispatch only) to combine the dispatched rows themselves
+ *                (identity experts).
  *  the rest      as for ep_layout.
  * Returns as the underlying calls do; on a non-zero return some work may
  * already be enqueued.
@@ -267,7 +270,8 @@ EP_API int ep_roundtrip_host(void* handle, void* stream, const void* x_host,
                              const int32_t* idx_host, const float* w_host, void* out_host,
                              int64_t T, int64_t H, int k, int E, int R, int kind, int capacity,
                              int64_t chunk_tokens, void* x_dev, int32_t* idx_dev, float* w_dev,
-                             void* recv, int64_t rows, const void* y, void* out_dev,
+                             void* recv, uint8_t* recv_q, float* recv_scale, int64_t rows,
+                             const void* y, void* out_dev,
                              int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
                              int32_t* rank_token_counts, uint32_t* status, void* workspace,
                              size_t workspace_bytes);

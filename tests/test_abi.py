@@ -107,8 +107,8 @@ def test_pipeline_argument_validation(lib):
     assert lib.ep_pipeline_create(0, ctypes.byref(ctypes.c_void_p())) == 1
     assert lib.ep_pipeline_create(5000, ctypes.byref(ctypes.c_void_p())) == 1
     assert lib.ep_pipeline_destroy(None) == 1
-    args = [FAKE] * 4 + [16, 64, 8, 256, 16, 0, 0, 4] + [FAKE] * 4 + [32, None, FAKE] + [FAKE] * 3 + \
-        [None, None, FAKE, 1 << 20]
+    args = [FAKE] * 4 + [16, 64, 8, 256, 16, 0, 0, 4] + [FAKE] * 4 + [None, None] + \
+        [32, None, FAKE] + [FAKE] * 3 + [None, None, FAKE, 1 << 20]
     assert lib.ep_roundtrip_host(None, None, *args) == 1     # no handle
 
 

@@ -67,3 +67,22 @@ def test_roundtrip_with_expert_outputs_on_device():
     used = lay.dst_row.view(-1).long()
     assert torch.equal(pipe.recv[used].view(torch.int16), recv_ref[used].view(torch.int16))
     pipe.close()
+
+
+def test_roundtrip_fp8_dispatch():
+    wl = W.WORKLOADS["prefill_fp8"].scaled(T=1500, H=1024)
+    x, idx, w = W.hidden_states(wl), W.route(wl), W.topk_weights(wl)
+    y = W.independent_expert_outputs(wl, device=DEV)
+    pipe = binding.Pipeline(wl.T, wl.H, wl.k, wl.E, wl.R, wl.kind, wl.capacity, chunk_tokens=400,
+                            device=DEV, y=y, payload="fp8")
+    oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+    pipe.run(x.pin_memory(), idx.pin_memory(), w.pin_memory(), oh)
+    torch.cuda.synchronize()
+    assert ep.status_read(pipe.layout.status) == 0
+    lay = ep.layout(idx.to(DEV), wl.E, wl.R, wl.kind, wl.capacity)
+    q, s = ep.dispatch_fp8(x.to(DEV), lay.dst_row, wl.rows)
+    used = lay.dst_row.view(-1).long()
+    assert torch.equal(pipe.recv_q[used], q[used]) and torch.equal(pipe.recv_scale[used], s[used])
+    ref = ep.combine(y, w.to(DEV), lay.dst_row).cpu()
+    assert torch.equal(oh.view(torch.int16), ref.view(torch.int16))
+    pipe.close()
