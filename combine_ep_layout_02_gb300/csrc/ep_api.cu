@@ -31,27 +31,6 @@ int check_rows_args(int64_t T, int64_t H, int k, int64_t rows) {
 
 namespace ep {
 void record_cuda_error(int err) { g_last_cuda_error = err; }
-
-int column_slices(int64_t T, int64_t max_slices) {
-    static int sm_count[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    if (sm_count[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            return 1;
-        sm_count[dev] = n;
-    }
-    if (T <= 0) return 1;
-    const int64_t want = (int64_t)sm_count[dev] * kTargetWarpsPerSM;
-    int64_t s = (want + T - 1) / T;
-    if (s > max_slices) s = max_slices;
-    if (s < 1) s = 1;
-    int p = 1;
-    while (p < s) p <<= 1;  // power of two, at most 2x the need
-    if (p > max_slices) p >>= 1;
-    return p < 1 ? 1 : p;
-}
 }  // namespace ep
 
 extern "C" {

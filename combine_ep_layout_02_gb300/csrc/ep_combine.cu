@@ -1,8 +1,7 @@
 // ep_combine.cu -- weighted top-k combine: out[t] = bf16(sum_j w[t,j] *
 // y[dst_row[t,j]]), accumulated in fp32 fused multiply-adds in increasing j.
 //
-// One warp per token (per column slice of a token when the batch is small).
-// Per iteration each lane owns 8 channels (one 16-byte
+// One warp per token.  Per iteration each lane owns 8 channels (one 16-byte
 // vector) of U column groups; the loads of all k rows for those groups are
 // issued before any arithmetic so that k*U 16-byte loads per lane are in
 // flight, then the FMAs run in j order (the order fixes the fp32 result
@@ -76,16 +75,12 @@ template <int U>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
                const int32_t* __restrict__ dst_row, int64_t T, int64_t nvec, int k, int64_t rows,
-               uint4* __restrict__ out, uint32_t* __restrict__ status, int slices,
-               int64_t slice_vec) {
+               uint4* __restrict__ out, uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-    const int64_t t = gw / slices;
+    const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     if (t >= T) return;  // warp-uniform
-    const int64_t v_begin = (gw % slices) * slice_vec;
-    const int64_t v_end = v_begin + slice_vec < nvec ? v_begin + slice_vec : nvec;
 
     int my_row = -1;
     float my_w = 0.0f;
@@ -111,19 +106,19 @@ combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
             wj[jj] = __shfl_sync(kFullMask, my_w, jj);
             src[jj] = (jj < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
         }
-        for (int64_t v0 = v_begin; v0 < v_end; v0 += 32 * U) {
+        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
             float acc[U][8];
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-            accumulate_batch<U>(src, wj, v0, v_end, lane, acc);
-            store_bf16<U>(out_row, v0, v_end, lane, acc);
+            accumulate_batch<U>(src, wj, v0, nvec, lane, acc);
+            store_bf16<U>(out_row, v0, nvec, lane, acc);
         }
         return;
     }
     // k > kRowBatch: batches of kRowBatch rows inside each column group
-    for (int64_t v0 = v_begin; v0 < v_end; v0 += 32 * U) {
+    for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
         float acc[U][8];
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -139,9 +134,9 @@ combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
                 wj[jj] = __shfl_sync(kFullMask, my_w, j & 31);
                 src[jj] = (j < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
             }
-            accumulate_batch<U>(src, wj, v0, v_end, lane, acc);
+            accumulate_batch<U>(src, wj, v0, nvec, lane, acc);
         }
-        store_bf16<U>(out_row, v0, v_end, lane, acc);
+        store_bf16<U>(out_row, v0, nvec, lane, acc);
     }
 }
 
@@ -152,15 +147,10 @@ cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* ds
                            cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const int64_t nvec = H / 8;
-    constexpr int64_t kIter = 32 * EP_COMBINE_U;  // vectors per warp iteration
-    const int64_t iters = (nvec + kIter - 1) / kIter;
-    const int slices = column_slices(T, iters);
-    const int64_t slice_vec = (iters + slices - 1) / slices * kIter;
-    const int64_t warps = T * slices;
-    const unsigned grid = (unsigned)((warps + kCombineWarps - 1) / kCombineWarps);
+    const unsigned grid = (unsigned)((T + kCombineWarps - 1) / kCombineWarps);
     return launch_pdl(combine_kernel<EP_COMBINE_U>, dim3(grid), dim3(kCombineWarps * 32), 0, stream,
                       static_cast<const uint4*>(y), topk_w, dst_row, T, nvec, k, rows,
-                      static_cast<uint4*>(out), status, slices, slice_vec);
+                      static_cast<uint4*>(out), status);
 }
 
 }  // namespace ep

@@ -1,8 +1,7 @@
 // ep_dispatch.cu -- dispatch (scatter of token rows into the per-expert
 // buffer), BF16 bit copy and the fused per-token FP8 e4m3 cast.
 //
-// One warp per token (per column slice of a token when the batch is small,
-// so that enough warps are in flight).  The warp reads the token row once in 16-byte vectors
+// One warp per token.  The warp reads the token row once in 16-byte vectors
 // (streaming, no L1 allocation) and writes it to each of its k destination
 // rows, so every input byte is read once and every output byte written once:
 // the HBM floor is T*H*2 read + T*k*H*2 (BF16) or T*k*(H + H/32) (FP8) written.
@@ -52,15 +51,12 @@ template <int U>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k,
                      const int32_t* __restrict__ dst_row, uint4* __restrict__ recv, int64_t rows,
-                     uint32_t* __restrict__ status, int slices, int64_t slice_vec) {
+                     uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
-    const int64_t t = gw / slices;
+    const int64_t t = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
     if (t >= T) return;  // warp-uniform
-    const int64_t v_begin = (gw % slices) * slice_vec;
-    const int64_t v_end = v_begin + slice_vec < nvec ? v_begin + slice_vec : nvec;
     const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const uint4* src = x + t * nvec;
     // k <= 8 is one pass; larger k re-reads the row once per 8 destinations
@@ -71,12 +67,12 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
             const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
             dst[jj] = (j0 + jj < k && r >= 0) ? recv + (int64_t)r * nvec : nullptr;
         }
-        for (int64_t v0 = v_begin; v0 < v_end; v0 += 32 * U) {
+        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
             uint4 buf[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + u * 32 + lane;
-                if (v < v_end) buf[u] = ld_stream_v4(src + v);
+                if (v < nvec) buf[u] = ld_stream_v4(src + v);
             }
 #pragma unroll
             for (int jj = 0; jj < kRowRegs; ++jj) {
@@ -84,7 +80,7 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t v = v0 + u * 32 + lane;
-                    if (v < v_end) {
+                    if (v < nvec) {
                         if (EP_DISPATCH_STORE_CS) st_cs_v4(dst[jj] + v, buf[u]);
                         else st_v4(dst[jj] + v, buf[u]);
                     }
@@ -100,16 +96,12 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
                     const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv_q,
-                    float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status,
-                    int slices, int64_t slice_ch) {
+                    float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
-    const int64_t t = gw / slices;
+    const int64_t t = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
     if (t >= T) return;
-    const int64_t c_begin = (gw % slices) * slice_ch;  // a multiple of 512 channels
-    const int64_t c_end = c_begin + slice_ch < H ? c_begin + slice_ch : H;
     const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const int64_t nblk = H / 128;
     const uint16_t* src = x + t * H;
@@ -120,9 +112,9 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
             const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
             rr[jj] = (j0 + jj < k) ? r : -1;
         }
-        for (int64_t c0 = c_begin; c0 < c_end; c0 += 512) {
+        for (int64_t c0 = 0; c0 < H; c0 += 512) {
             const int64_t c = c0 + lane * 16;
-            const bool act = c < c_end;  // c_end % 128 == 0: all 8 lanes of a block agree
+            const bool act = c < H;  // H % 128 == 0: all 8 lanes of a block agree
             uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
             if (act) {
                 a = ld_stream_v4(src + c);
@@ -263,29 +255,20 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
     }
 #endif
     const int64_t nvec = H / 8;
-    constexpr int64_t kIter = 32 * EP_DISPATCH_U;  // vectors per warp iteration
-    const int64_t iters = (nvec + kIter - 1) / kIter;
-    const int slices = column_slices(T, iters);
-    const int64_t slice_vec = (iters + slices - 1) / slices * kIter;
-    const int64_t warps = T * slices;
-    const unsigned grid = (unsigned)((warps + kDispatchWarps - 1) / kDispatchWarps);
-    return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U>, dim3(grid), dim3(kDispatchWarps * 32), 0,
-                      stream, static_cast<const uint4*>(x), T, nvec, k, dst_row,
-                      static_cast<uint4*>(recv), rows, status, slices, slice_vec);
+    const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
+    return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U>, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
+                      static_cast<const uint4*>(x), T, nvec, k, dst_row, static_cast<uint4*>(recv),
+                      rows, status);
 }
 
 cudaError_t launch_dispatch_fp8(const void* x, int64_t T, int64_t H, int k,
                                 const int32_t* dst_row, uint8_t* recv_q, float* recv_scale,
                                 int64_t rows, uint32_t* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const int64_t iters = (H + 511) / 512;  // 512 channels per warp iteration
-    const int slices = column_slices(T, iters);
-    const int64_t slice_ch = (iters + slices - 1) / slices * 512;
-    const int64_t warps = T * slices;
-    const unsigned grid = (unsigned)((warps + kDispatchWarps - 1) / kDispatchWarps);
+    const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
     return launch_pdl(dispatch_fp8_kernel, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
                       static_cast<const uint16_t*>(x), T, H, k, dst_row, recv_q, recv_scale, rows,
-                      status, slices, slice_ch);
+                      status);
 }
 
 }  // namespace ep

@@ -189,13 +189,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Column slices per token for the dispatch / combine kernels: small batches
-// get several warps per token (each on a slice of the columns) so that about
-// kTargetWarpsPerSM warps per SM have work; large batches keep one warp per
-// token.  `max_slices` bounds the split (slices stay whole warp iterations).
-constexpr int kTargetWarpsPerSM = 48;
-int column_slices(int64_t T, int64_t max_slices);
-
 // Tokens per layout chunk (one per thread of a 128-thread block).
 constexpr int kLayoutThreads = 128;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
