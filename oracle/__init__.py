@@ -44,6 +44,14 @@ def _load():
         lib.oracle_layout.restype = ctypes.c_uint32
         lib.oracle_layout_aligned.argtypes = [P, i64, i32, i32, i32, i32, P, P, P, P]
         lib.oracle_layout_aligned.restype = ctypes.c_uint32
+        lib.oracle_rank_layout.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P]
+        lib.oracle_rank_layout.restype = ctypes.c_uint32
+        lib.oracle_expand.argtypes = [P, P, P, i64, i64, i32, P]
+        lib.oracle_expand.restype = None
+        lib.oracle_combine_partial.argtypes = [P, P, P, P, P, i64, i64, i32, P]
+        lib.oracle_combine_partial.restype = None
+        lib.oracle_combine_reduce.argtypes = [P, P, i64, i64, i32, P]
+        lib.oracle_combine_reduce.restype = None
         lib.oracle_dispatch_bf16.argtypes = [P, i64, i64, i32, P, P]
         lib.oracle_dispatch_bf16.restype = None
         lib.oracle_quantize_row_fp8.argtypes = [P, i64, P, P]
@@ -188,6 +196,62 @@ def combine_fp32_seq(y, topk_w, dst_row):
     return out
 
 
+# --- two-stage (rank, then expert) path ------------------------------------
+
+def rank_layout(topk_idx, E, R):
+    """Returns dict(rank_counts, rank_offsets, rank_dst_row, pair_rank_row,
+    rank_row_token, flags); rank_row_token has rank_offsets[R] entries."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    rc = np.zeros(R, np.int32)
+    ro = np.zeros(R + 1, np.int32)
+    rdst = np.zeros((T, k), np.int32)
+    prr = np.zeros((T, k), np.int32)
+    tok = np.full(max(1, T * min(k, R)), -1, np.int32)
+    flags = _load().oracle_rank_layout(_p(idx), T, k, E, R, _p(rc), _p(ro), _p(rdst), _p(prr), _p(tok))
+    if flags == 0xFFFFFFFF:
+        raise ValueError("oracle_rank_layout: invalid sizes")
+    return dict(rank_counts=rc, rank_offsets=ro, rank_dst_row=rdst, pair_rank_row=prr,
+                rank_row_token=tok[:int(ro[R])], flags=int(flags))
+
+
+def expand(rank_buf, pair_rank_row, dst_row, rows, recv=None):
+    rank_buf = _c(rank_buf, np.uint16)
+    prr = _c(pair_rank_row, np.int32)
+    dst = _c(dst_row, np.int32)
+    T, k = dst.shape
+    H = rank_buf.shape[1]
+    if recv is None:
+        recv = np.zeros((rows, H), np.uint16)
+    _load().oracle_expand(_p(rank_buf), _p(prr), _p(dst), T, H, k, _p(recv))
+    return recv
+
+
+def combine_partial(y, topk_w, dst_row, pair_rank_row, rank_row_token):
+    y = _c(y, np.uint16)
+    w = _c(topk_w, np.float32)
+    dst = _c(dst_row, np.int32)
+    prr = _c(pair_rank_row, np.int32)
+    tok = _c(rank_row_token, np.int32)
+    k = dst.shape[1]
+    H = y.shape[1]
+    n = tok.shape[0]
+    part = np.zeros((max(n, 1), H), np.uint16)
+    _load().oracle_combine_partial(_p(y), _p(w), _p(dst), _p(prr), _p(tok), n, H, k, _p(part))
+    return part[:n]
+
+
+def combine_reduce(partial, rank_dst_row, H):
+    part = _c(partial, np.uint16)
+    rdst = _c(rank_dst_row, np.int32)
+    T, k = rdst.shape
+    out = np.zeros((T, H), np.uint16)
+    if part.size == 0:
+        part = np.zeros((1, H), np.uint16)
+    _load().oracle_combine_reduce(_p(part), _p(rdst), T, H, k, _p(out))
+    return out
+
+
 def library_path():
     return _build.build()
 
@@ -196,5 +260,6 @@ __all__ = [
     "LAYOUT_CONTIGUOUS", "LAYOUT_MASKED", "FLAG_BAD_EXPERT", "FLAG_OVERFLOW",
     "bf16_to_float", "bf16_from_double", "e4m3_decode", "e4m3_encode",
     "layout", "layout_aligned", "dispatch_bf16", "quantize_row_fp8", "dispatch_fp8",
-    "combine_f64", "combine_fp32_seq", "library_path",
+    "combine_f64", "combine_fp32_seq", "rank_layout", "expand", "combine_partial",
+    "combine_reduce", "library_path",
 ]

@@ -319,3 +319,122 @@ void oracle_combine_fp32_seq(const uint16_t* y, const float* topk_w,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Two-stage path: one copy per (token, virtual rank), then expansion into  */
+/* the experts of that rank; rank-local partial sums, then a final sum.     */
+/* ------------------------------------------------------------------------ */
+
+/* The pages' transport sends one copy of a token per destination rank and
+ * expands it into that rank's experts on arrival (afdEP record, kernel
+ * traces: dispatch_copy_epilogue; PR #1238 methodology review: one copy per
+ * destination node, then forwarding to the local experts).  Plain
+ * definition: tokens in order; within a token the ranks in order of their
+ * first pair j; rank r's rows in token order. */
+uint32_t oracle_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                            int32_t* rank_counts, int32_t* rank_offsets,
+                            int32_t* rank_dst_row, int32_t* pair_rank_row,
+                            int32_t* rank_row_token) {
+    if (T < 0 || k < 1 || E < 1 || R < 1 || E % R != 0) return 0xFFFFFFFFu;
+    int per_rank = E / R;
+    uint32_t flags = 0;
+    int64_t npairs = T * (int64_t)k;
+    int64_t* cnt = (int64_t*)calloc((size_t)R, sizeof(int64_t));
+    int64_t* slot = (int64_t*)malloc((size_t)(npairs > 0 ? npairs : 1) * sizeof(int64_t));
+    /* pass 1: a slot for the first pair of each (token, rank) */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t p = t * k + j;
+            int32_t e = topk_idx[p];
+            slot[p] = -1;
+            if (e < 0 || e >= E) {
+                if (e != -1) flags |= ORACLE_FLAG_BAD_EXPERT;
+                continue;
+            }
+            int r = e / per_rank;
+            int first = 1;
+            for (int jj = 0; jj < j; ++jj) {
+                int32_t e2 = topk_idx[t * k + jj];
+                if (e2 >= 0 && e2 < E && e2 / per_rank == r) first = 0;
+            }
+            if (first) slot[p] = cnt[r]++;
+        }
+    }
+    int64_t run = 0;
+    for (int r = 0; r < R; ++r) {
+        rank_counts[r] = (int32_t)cnt[r];
+        rank_offsets[r] = (int32_t)run;
+        run += cnt[r];
+    }
+    rank_offsets[R] = (int32_t)run;
+    /* pass 2: rows */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t p = t * k + j;
+            int32_t e = topk_idx[p];
+            rank_dst_row[p] = -1;
+            pair_rank_row[p] = -1;
+            if (e < 0 || e >= E) continue;
+            int r = e / per_rank;
+            if (slot[p] >= 0) {
+                int32_t row = (int32_t)(rank_offsets[r] + slot[p]);
+                rank_dst_row[p] = row;
+                pair_rank_row[p] = row;
+                rank_row_token[row] = (int32_t)t;
+            } else {
+                for (int jj = 0; jj < j; ++jj)
+                    if (rank_dst_row[t * k + jj] >= 0 && topk_idx[t * k + jj] / per_rank == r)
+                        pair_rank_row[p] = rank_dst_row[t * k + jj];
+            }
+        }
+    }
+    free(slot);
+    free(cnt);
+    return flags;
+}
+
+void oracle_expand(const uint16_t* rank_buf, const int32_t* pair_rank_row,
+                   const int32_t* dst_row, int64_t T, int64_t H, int k, uint16_t* recv) {
+    for (int64_t p = 0; p < T * k; ++p) {
+        if (pair_rank_row[p] < 0 || dst_row[p] < 0) continue;
+        for (int64_t h = 0; h < H; ++h)
+            recv[(int64_t)dst_row[p] * H + h] = rank_buf[(int64_t)pair_rank_row[p] * H + h];
+    }
+}
+
+/* The rank-local half of the combine (the pages' combine sends BF16 rows
+ * back; each is the reduction over the token's experts on that rank). */
+void oracle_combine_partial(const uint16_t* y, const float* topk_w,
+                            const int32_t* dst_row, const int32_t* pair_rank_row,
+                            const int32_t* rank_row_token, int64_t n_rows, int64_t H,
+                            int k, uint16_t* partial) {
+    for (int64_t i = 0; i < n_rows; ++i) {
+        int64_t t = rank_row_token[i];
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                int64_t p = t * k + j;
+                if (pair_rank_row[p] != i || dst_row[p] < 0) continue;
+                acc = fmaf(topk_w[p], oracle_bf16_to_float(y[(int64_t)dst_row[p] * H + h]), acc);
+            }
+            partial[i * H + h] = oracle_bf16_from_double((double)acc);
+        }
+    }
+}
+
+/* The final reduction over a token's ranks (combine_reduce_epilogue in the
+ * afdEP kernel traces). */
+void oracle_combine_reduce(const uint16_t* partial, const int32_t* rank_dst_row,
+                           int64_t T, int64_t H, int k, uint16_t* out) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                int32_t row = rank_dst_row[t * k + j];
+                if (row < 0) continue;
+                acc = acc + oracle_bf16_to_float(partial[(int64_t)row * H + h]);
+            }
+            out[t * H + h] = oracle_bf16_from_double((double)acc);
+        }
+    }
+}

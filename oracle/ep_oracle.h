@@ -77,6 +77,35 @@ void oracle_combine_fp32_seq(const uint16_t* y, const float* topk_w,
                              const int32_t* dst_row, int64_t T, int64_t H,
                              int k, uint16_t* out);
 
+/* ---- two-stage (rank, then expert) path ---------------------------------
+ * Rank layout: every (token t, virtual rank r) that t reaches gets one row of
+ * a rank buffer, rank r's rows in token order.  rank_dst_row[t,j] is that row
+ * for the FIRST pair of t in rank r and -1 for its other pairs (and for
+ * pairs with no valid expert); pair_rank_row[t,j] is the row for every pair
+ * with a valid expert.  rank_row_token[row] is the row's token. */
+uint32_t oracle_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                            int32_t* rank_counts, int32_t* rank_offsets,
+                            int32_t* rank_dst_row, int32_t* pair_rank_row,
+                            int32_t* rank_row_token);
+
+/* Expansion: recv[dst_row[t,j]] = rank_buf[pair_rank_row[t,j]] for every
+ * pair with both rows valid. */
+void oracle_expand(const uint16_t* rank_buf, const int32_t* pair_rank_row,
+                   const int32_t* dst_row, int64_t T, int64_t H, int k, uint16_t* recv);
+
+/* Rank-local partial reduction: partial[i] = bf16(fp32 fma chain over the
+ * pairs j (increasing) of token rank_row_token[i] with pair_rank_row == i and
+ * dst_row >= 0 of w[t,j] * y[dst_row[t,j]]), for i < n_rows. */
+void oracle_combine_partial(const uint16_t* y, const float* topk_w,
+                            const int32_t* dst_row, const int32_t* pair_rank_row,
+                            const int32_t* rank_row_token, int64_t n_rows, int64_t H,
+                            int k, uint16_t* partial);
+
+/* Final reduction: out[t] = bf16(fp32 sum, in increasing j, of
+ * partial[rank_dst_row[t,j]] over the pairs with rank_dst_row >= 0). */
+void oracle_combine_reduce(const uint16_t* partial, const int32_t* rank_dst_row,
+                           int64_t T, int64_t H, int k, uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif
