@@ -57,6 +57,11 @@ def load():
         "ep_layout_aligned": ([P, i64, i32, i32, i32, i32, P, P, P, P, P, P, sz, P], i32),
         "ep_layout_static_ws": ([P, i64, i32, i32, i32, i32, i32, P, P, P, P, P, P], i32),
         "ep_dispatch": ([P, i64, i64, i32, P, P, i64, P, P], i32),
+        "ep_rank_layout_workspace_bytes": ([i64, i32, i32, i32], sz),
+        "ep_rank_layout": ([P, i64, i32, i32, i32, P, P, P, P, P, i64, P, P, sz, P], i32),
+        "ep_expand": ([P, P, i32, i64, P, P, P, i64, i64, i32, P, i64, P, P], i32),
+        "ep_combine_partial": ([P, i64, P, P, P, P, P, i32, i64, i64, i64, i32, P, P, P], i32),
+        "ep_combine_reduce": ([P, i64, P, i64, i64, i32, P, P, P], i32),
         "ep_dispatch_fp8": ([P, i64, i64, i32, P, P, P, i64, P, P], i32),
         "ep_combine": ([P, P, P, i64, i64, i32, i64, P, P, P], i32),
         "ep_status_read": ([P, P, P], i32),
@@ -217,6 +222,85 @@ def combine(y, topk_w, dst_row, out=None, status=None):
     code = load().ep_combine(_ptr(y), _ptr(topk_w), _ptr(dst_row), T, H, k, rows, _ptr(out),
                              _ptr(status), _stream(y.device))
     _rc("ep_combine", code)
+    return out
+
+
+RankLayoutOut = namedtuple("RankLayoutOut",
+                           "rank_counts rank_offsets rank_dst_row pair_rank_row rank_row_token status")
+
+
+def rank_rows_bound(T, k, R):
+    """Rows a rank buffer needs for any route: one per (token, rank) reached."""
+    return T * min(k, R)
+
+
+def rank_layout(topk_idx, E, R, *, out=None, workspace=None):
+    """Two-stage layout (see ``ep_rank_layout``)."""
+    _check_dev("topk_idx", topk_idx, torch.int32)
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    cap = rank_rows_bound(T, k, R)
+    if out is None:
+        out = RankLayoutOut(torch.empty(R, dtype=torch.int32, device=dev),
+                            torch.empty(R + 1, dtype=torch.int32, device=dev),
+                            torch.empty(T, k, dtype=torch.int32, device=dev),
+                            torch.empty(T, k, dtype=torch.int32, device=dev),
+                            torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                            torch.empty(1, dtype=torch.int32, device=dev))
+    need = int(load().ep_rank_layout_workspace_bytes(T, k, E, R))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() if workspace is not None else 0
+    code = load().ep_rank_layout(_ptr(topk_idx), T, k, E, R, _ptr(out.rank_counts),
+                                 _ptr(out.rank_offsets), _ptr(out.rank_dst_row),
+                                 _ptr(out.pair_rank_row), _ptr(out.rank_row_token),
+                                 out.rank_row_token.numel(), _ptr(out.status), _ptr(workspace),
+                                 wbytes, _stream(dev))
+    _rc("ep_rank_layout", code)
+    return out
+
+
+def expand(rank_buf, rl, dst_row, rows, recv=None, status=None):
+    """Expansion of rank rows into the expert rows (see ``ep_expand``)."""
+    _check_dev("rank_buf", rank_buf, torch.bfloat16)
+    T, k = dst_row.shape
+    H = rank_buf.shape[1]
+    R = rl.rank_counts.numel()
+    if recv is None:
+        recv = torch.empty(rows, H, dtype=torch.bfloat16, device=rank_buf.device)
+    code = load().ep_expand(_ptr(rank_buf), _ptr(rl.rank_offsets), R, rank_buf.shape[0],
+                            _ptr(rl.rank_row_token), _ptr(rl.pair_rank_row), _ptr(dst_row), T, H,
+                            k, _ptr(recv), rows, _ptr(status), _stream(rank_buf.device))
+    _rc("ep_expand", code)
+    return recv
+
+
+def combine_partial(y, topk_w, dst_row, rl, rank_rows, partial=None, status=None):
+    """Rank-local partial reduction (see ``ep_combine_partial``)."""
+    _check_dev("y", y, torch.bfloat16)
+    T, k = dst_row.shape
+    H = y.shape[1]
+    R = rl.rank_counts.numel()
+    if partial is None:
+        partial = torch.empty(max(rank_rows, 1), H, dtype=torch.bfloat16, device=y.device)
+    code = load().ep_combine_partial(_ptr(y), y.shape[0], _ptr(topk_w), _ptr(dst_row),
+                                     _ptr(rl.pair_rank_row), _ptr(rl.rank_row_token),
+                                     _ptr(rl.rank_offsets), R, rank_rows, T, H, k, _ptr(partial),
+                                     _ptr(status), _stream(y.device))
+    _rc("ep_combine_partial", code)
+    return partial
+
+
+def combine_reduce(partial, rl, T, out=None, status=None):
+    """Final reduction over each token's rank rows (see ``ep_combine_reduce``)."""
+    _check_dev("partial", partial, torch.bfloat16)
+    H = partial.shape[1]
+    k = rl.rank_dst_row.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=partial.device)
+    code = load().ep_combine_reduce(_ptr(partial), partial.shape[0], _ptr(rl.rank_dst_row), T, H,
+                                    k, _ptr(out), _ptr(status), _stream(partial.device))
+    _rc("ep_combine_reduce", code)
     return out
 
 

@@ -150,6 +150,88 @@ int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row, int64
                                           as_stream(stream)));
 }
 
+size_t ep_rank_layout_workspace_bytes(int64_t T, int k, int E, int R) {
+    if (T <= 0 || k < 1 || E < 1 || R < 1) return 0;
+    return ep::rank_keys_bytes(T, k) + ep_layout_workspace_bytes(T, k, R, 1, 0);
+}
+
+int ep_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                   int32_t* rank_counts, int32_t* rank_offsets, int32_t* rank_dst_row,
+                   int32_t* pair_rank_row, int32_t* rank_row_token, int64_t rank_rows,
+                   uint32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+    if (T < 0 || k < 1 || k > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || E % R != 0)
+        return EP_ERR_INVALID_ARG;
+    if (T > (int64_t)INT32_MAX / k) return EP_ERR_INVALID_ARG;
+    if (!rank_counts || !rank_offsets || rank_rows < 0) return EP_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !rank_dst_row || !pair_rank_row || !rank_row_token))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(topk_idx, 4) || !aligned(rank_counts, 4) || !aligned(rank_offsets, 4) ||
+        !aligned(rank_dst_row, 4) || !aligned(pair_rank_row, 4) || !aligned(rank_row_token, 4) ||
+        !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    const size_t need = ep_rank_layout_workspace_bytes(T, k, E, R);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return EP_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return EP_ERR_ALIGNMENT;
+    }
+    return cuda_status(ep::launch_rank_layout(topk_idx, T, k, E, R, rank_counts, rank_offsets,
+                                              rank_dst_row, pair_rank_row, rank_row_token,
+                                              rank_rows, status, workspace, as_stream(stream)));
+}
+
+int ep_expand(const void* rank_buf, const int32_t* rank_offsets, int R, int64_t rank_rows,
+              const int32_t* rank_row_token, const int32_t* pair_rank_row,
+              const int32_t* dst_row, int64_t T, int64_t H, int k, void* recv, int64_t rows,
+              uint32_t* status, void* stream) {
+    int rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (R < 1 || rank_rows < 0 || rank_rows > (int64_t)INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (T == 0 || rank_rows == 0) return EP_OK;
+    if (!rank_buf || !rank_offsets || !rank_row_token || !pair_rank_row || !dst_row ||
+        (!recv && rows > 0))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(rank_buf, 16) || !aligned(recv, 16) || !aligned(rank_offsets, 4) ||
+        !aligned(rank_row_token, 4) || !aligned(pair_rank_row, 4) || !aligned(dst_row, 4) ||
+        !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(ep::launch_expand(rank_buf, rank_offsets, R, rank_rows, rank_row_token,
+                                         pair_rank_row, dst_row, T, H, k, recv, rows, status,
+                                         as_stream(stream)));
+}
+
+int ep_combine_partial(const void* y, int64_t rows, const float* topk_w, const int32_t* dst_row,
+                       const int32_t* pair_rank_row, const int32_t* rank_row_token,
+                       const int32_t* rank_offsets, int R, int64_t rank_rows, int64_t T,
+                       int64_t H, int k, void* partial, uint32_t* status, void* stream) {
+    int rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (R < 1 || rank_rows < 0 || rank_rows > (int64_t)INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (T == 0 || rank_rows == 0) return EP_OK;
+    if (!topk_w || !dst_row || !pair_rank_row || !rank_row_token || !rank_offsets || !partial ||
+        (!y && rows > 0))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(y, 16) || !aligned(partial, 16) || !aligned(topk_w, 4) || !aligned(dst_row, 4) ||
+        !aligned(pair_rank_row, 4) || !aligned(rank_row_token, 4) || !aligned(rank_offsets, 4) ||
+        !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(ep::launch_combine_partial(y, rows, topk_w, dst_row, pair_rank_row,
+                                                  rank_row_token, rank_offsets, R, rank_rows, T,
+                                                  H, k, partial, status, as_stream(stream)));
+}
+
+int ep_combine_reduce(const void* partial, int64_t rank_rows, const int32_t* rank_dst_row,
+                      int64_t T, int64_t H, int k, void* out, uint32_t* status, void* stream) {
+    int rc = check_rows_args(T, H, k, rank_rows);
+    if (rc != EP_OK) return rc;
+    if (T == 0) return EP_OK;
+    if (!rank_dst_row || !out || (!partial && rank_rows > 0)) return EP_ERR_INVALID_ARG;
+    if (!aligned(partial, 16) || !aligned(out, 16) || !aligned(rank_dst_row, 4) ||
+        !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(ep::launch_combine_reduce(partial, rank_rows, rank_dst_row, T, H, k, out,
+                                                 status, as_stream(stream)));
+}
+
 int ep_status_read(const uint32_t* status, void* stream, uint32_t* host_flags) {
     if (!status || !host_flags) return EP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemcpyAsync(host_flags, status, sizeof(uint32_t), cudaMemcpyDeviceToHost,

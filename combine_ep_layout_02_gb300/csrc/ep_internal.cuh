@@ -215,4 +215,24 @@ cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* ds
                            int64_t H, int k, int64_t rows, void* out, uint32_t* status,
                            cudaStream_t stream);
 
+// two-stage (rank, then expert) path
+size_t rank_keys_bytes(int64_t T, int k);
+cudaError_t launch_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                               int32_t* rank_counts, int32_t* rank_offsets,
+                               int32_t* rank_dst_row, int32_t* pair_rank_row,
+                               int32_t* rank_row_token, int64_t cap, uint32_t* status,
+                               void* workspace, cudaStream_t stream);
+cudaError_t launch_expand(const void* rank_buf, const int32_t* rank_offsets, int R, int64_t cap,
+                          const int32_t* rank_row_token, const int32_t* pair_rank_row,
+                          const int32_t* dst_row, int64_t T, int64_t H, int k, void* recv,
+                          int64_t rows, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_combine_partial(const void* y, int64_t rows, const float* topk_w,
+                                   const int32_t* dst_row, const int32_t* pair_rank_row,
+                                   const int32_t* rank_row_token, const int32_t* rank_offsets,
+                                   int R, int64_t cap, int64_t T, int64_t H, int k, void* partial,
+                                   uint32_t* status, cudaStream_t stream);
+cudaError_t launch_combine_reduce(const void* partial, int64_t cap, const int32_t* rank_dst_row,
+                                  int64_t T, int64_t H, int k, void* out, uint32_t* status,
+                                  cudaStream_t stream);
+
 }  // namespace ep

@@ -1,0 +1,357 @@
+// ep_two_stage.cu -- the two-stage (rank, then expert) form of dispatch and
+// combine that the pages' transport uses: one copy of a token per virtual
+// rank it reaches, expanded on arrival into that rank's experts
+// (dispatch_copy_epilogue in the afdEP kernel traces), and on the way back a
+// rank-local partial reduction followed by the final reduction over the
+// token's ranks (combine_reduce_epilogue).  Here the "ranks" are regions of
+// one GPU's memory, so the copy to ranks is ep_dispatch with rank_dst_row.
+//
+//   rank layout : keys kernel (one key per (token, rank): the rank for the
+//                 token's first pair in that rank, -1 for its other pairs)
+//                 -> the ordinary layout over keys with E' = R experts
+//                 -> finish kernel (pair_rank_row for every pair, the token
+//                 of every rank row).
+//   expand      : one warp per rank row, copying it to the expert rows of its
+//                 token's pairs in that rank.
+//   partial     : one warp per rank row, fp32 FMA chain over those pairs in
+//                 increasing j, rounded to bf16.
+//   reduce      : one warp per token, fp32 sum of its rank rows' partials in
+//                 increasing j of their first pair, rounded to bf16.
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kWarps = 8;
+
+// Keys for the rank layout: the rank for the first pair of each (token,
+// rank), -1 for the token's other pairs in that rank and for id -1, and R
+// (out of range for the inner layout, which flags it) for any other bad id.
+__global__ void rank_keys_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, int R,
+                                 int32_t* __restrict__ keys) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const int per_rank = E / R;
+    const int32_t* row = idx + t * k;
+    int32_t* out = keys + t * k;
+    uint64_t seen = 0;  // ranks < 64 already keyed for this token
+    for (int j = 0; j < k; ++j) {
+        const int e = row[j];
+        int key;
+        if (e == -1) {
+            key = -1;
+        } else if (e < -1 || e >= E) {
+            key = R;
+        } else {
+            const int r = e / per_rank;
+            bool first;
+            if (r < 64) {
+                first = !((seen >> r) & 1);
+                seen |= 1ull << r;
+            } else {
+                first = true;
+                for (int jj = 0; jj < j; ++jj) {
+                    const int e2 = row[jj];
+                    if (e2 >= 0 && e2 < E && e2 / per_rank == r) { first = false; break; }
+                }
+            }
+            key = first ? r : -1;
+        }
+        out[j] = key;
+    }
+}
+
+// pair_rank_row for every pair and the token of every rank row.
+__global__ void rank_finish_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, int R,
+                                   const int32_t* __restrict__ rank_dst_row,
+                                   int32_t* __restrict__ pair_rank_row,
+                                   int32_t* __restrict__ rank_row_token, int64_t cap,
+                                   uint32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const int per_rank = E / R;
+    const int32_t* row = idx + t * k;
+    const int32_t* rdst = rank_dst_row + t * k;
+    for (int j = 0; j < k; ++j) {
+        const int e = row[j];
+        int out = -1;
+        const int first_row = rdst[j];
+        if (first_row >= 0) {
+            out = first_row;
+            if (first_row < cap) rank_row_token[first_row] = (int32_t)t;
+            else if (status) atomicOr(status, EP_FLAG_BAD_ROW);  // caller's buffer too small
+        } else if (e >= 0 && e < E) {
+            const int r = e / per_rank;
+            for (int jj = 0; jj < j; ++jj) {
+                const int e2 = row[jj];
+                if (rdst[jj] >= 0 && e2 / per_rank == r) { out = rdst[jj]; break; }
+            }
+        }
+        pair_rank_row[t * k + j] = out;
+    }
+}
+
+// The pairs of rank row i's token that belong to row i: lane j (< k) returns
+// its destination row (validated against [0, rows)) or -1.
+__device__ __forceinline__ int rank_row_pair(int64_t i, int64_t t, int k,
+                                             const int32_t* __restrict__ pair_rank_row,
+                                             const int32_t* __restrict__ dst_row, int64_t rows,
+                                             uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    int d = -1;
+    bool bad = false;
+    if (lane < k) {
+        const int pr = __ldg(pair_rank_row + t * k + lane);
+        const int dd = __ldg(dst_row + t * k + lane);
+        if (dd < -1 || (int64_t)dd >= rows) bad = true;
+        else if (pr == i) d = dd;
+    }
+    warp_flag(status, bad, EP_FLAG_BAD_ROW);
+    return d;
+}
+
+// Number of rank rows (rank_offsets[R]); rows beyond `cap` are not touched
+// and raise EP_FLAG_BAD_ROW.
+__device__ __forceinline__ int64_t live_rank_rows(const int32_t* rank_offsets, int R, int64_t cap,
+                                                  uint32_t* status) {
+    int64_t n = __ldg(rank_offsets + R);
+    if (n > cap) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && status) atomicOr(status, EP_FLAG_BAD_ROW);
+        n = cap;
+    }
+    return n;
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+expand_kernel(const uint4* __restrict__ rank_buf, const int32_t* __restrict__ rank_offsets, int R,
+              int64_t cap, const int32_t* __restrict__ rank_row_token,
+              const int32_t* __restrict__ pair_rank_row, const int32_t* __restrict__ dst_row,
+              int64_t T, int64_t nvec, int k, uint4* __restrict__ recv, int64_t rows,
+              uint32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t i = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (i >= live_rank_rows(rank_offsets, R, cap, status)) return;  // warp-uniform
+    const int64_t t = __ldg(rank_row_token + i);
+    if (t < 0 || t >= T) {
+        if (lane == 0 && status) atomicOr(status, EP_FLAG_BAD_ROW);
+        return;
+    }
+    const int my_row = rank_row_pair(i, t, k, pair_rank_row, dst_row, rows, status);
+    const uint4* src = rank_buf + i * nvec;
+    constexpr int U = 4;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        uint4* dst[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
+            dst[jj] = (j0 + jj < k && r >= 0) ? recv + (int64_t)r * nvec : nullptr;
+        }
+        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+            uint4 buf[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * 32 + lane;
+                if (v < nvec) buf[u] = ld_stream_v4(src + v);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (dst[jj] == nullptr) continue;  // warp-uniform
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = v0 + u * 32 + lane;
+                    if (v < nvec) st_v4(dst[jj] + v, buf[u]);
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* __restrict__ topk_w,
+                       const int32_t* __restrict__ dst_row,
+                       const int32_t* __restrict__ pair_rank_row,
+                       const int32_t* __restrict__ rank_row_token,
+                       const int32_t* __restrict__ rank_offsets, int R, int64_t cap, int64_t T,
+                       int64_t nvec, int k, uint4* __restrict__ partial,
+                       uint32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t i = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (i >= live_rank_rows(rank_offsets, R, cap, status)) return;
+    const int64_t t = __ldg(rank_row_token + i);
+    if (t < 0 || t >= T) {
+        if (lane == 0 && status) atomicOr(status, EP_FLAG_BAD_ROW);
+        return;
+    }
+    const int my_row = rank_row_pair(i, t, k, pair_rank_row, dst_row, rows, status);
+    const float my_w = lane < k ? __ldg(topk_w + t * k + lane) : 0.0f;
+    uint4* out_row = partial + i * nvec;
+    for (int64_t v0 = 0; v0 < nvec; v0 += 64) {  // two 16-byte vectors per lane
+        float acc[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int r = __shfl_sync(kFullMask, my_row, j);
+            const float w = __shfl_sync(kFullMask, my_w, j);
+            if (r < 0) continue;  // warp-uniform
+            const uint4* src = y + (int64_t)r * nvec;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t v = v0 + u * 32 + lane;
+                if (v >= nvec) continue;
+                const uint4 b = ld_stream_v4(src + v);
+                const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[u][2 * q] = __fmaf_rn(w, bf16lo_to_f32(wv[q]), acc[u][2 * q]);
+                    acc[u][2 * q + 1] = __fmaf_rn(w, bf16hi_to_f32(wv[q]), acc[u][2 * q + 1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t v = v0 + u * 32 + lane;
+            if (v < nvec) {
+                uint4 o;
+                o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
+                o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
+                o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
+                o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
+                st_v4(out_row + v, o);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+combine_reduce_kernel(const uint4* __restrict__ partial, int64_t cap,
+                      const int32_t* __restrict__ rank_dst_row, int64_t T, int64_t nvec, int k,
+                      uint4* __restrict__ out, uint32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_row = -1;
+    bool bad = false;
+    if (lane < k) {
+        my_row = __ldg(rank_dst_row + t * k + lane);
+        if (my_row < -1 || (int64_t)my_row >= cap) {
+            bad = true;
+            my_row = -1;
+        }
+    }
+    warp_flag(status, bad, EP_FLAG_BAD_ROW);
+    uint4* out_row = out + t * nvec;
+    for (int64_t v0 = 0; v0 < nvec; v0 += 64) {
+        float acc[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int r = __shfl_sync(kFullMask, my_row, j);
+            if (r < 0) continue;  // warp-uniform
+            const uint4* src = partial + (int64_t)r * nvec;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t v = v0 + u * 32 + lane;
+                if (v >= nvec) continue;
+                const uint4 b = ld_stream_v4(src + v);
+                const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[u][2 * q] = __fadd_rn(acc[u][2 * q], bf16lo_to_f32(wv[q]));
+                    acc[u][2 * q + 1] = __fadd_rn(acc[u][2 * q + 1], bf16hi_to_f32(wv[q]));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t v = v0 + u * 32 + lane;
+            if (v < nvec) {
+                uint4 o;
+                o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
+                o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
+                o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
+                o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
+                st_v4(out_row + v, o);
+            }
+        }
+    }
+}
+
+inline unsigned blocks_for(int64_t n, int per_block) {
+    return (unsigned)((n + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+size_t rank_keys_bytes(int64_t T, int k) {
+    return ((size_t)T * k * sizeof(int32_t) + 255) & ~(size_t)255;
+}
+
+cudaError_t launch_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                               int32_t* rank_counts, int32_t* rank_offsets,
+                               int32_t* rank_dst_row, int32_t* pair_rank_row,
+                               int32_t* rank_row_token, int64_t cap, uint32_t* status,
+                               void* workspace, cudaStream_t stream) {
+    int32_t* keys = static_cast<int32_t*>(workspace);
+    int32_t* inner_ws =
+        reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + rank_keys_bytes(T, k));
+    cudaError_t e;
+    if (T > 0) {
+        e = launch_pdl(rank_keys_kernel, dim3(blocks_for(T, 256)), dim3(256), 0, stream, topk_idx,
+                       T, k, E, R, keys);
+        if (e != cudaSuccess) return e;
+    }
+    // the ordinary layout over the keys: R "experts", one virtual rank
+    e = launch_layout(keys, T, k, R, 1, EP_LAYOUT_CONTIGUOUS, 0, 1, rank_counts, rank_offsets,
+                      rank_dst_row, nullptr, status, inner_ws, stream);
+    if (e != cudaSuccess || T == 0) return e;
+    return launch_pdl(rank_finish_kernel, dim3(blocks_for(T, 256)), dim3(256), 0, stream,
+                      topk_idx, T, k, E, R, (const int32_t*)rank_dst_row, pair_rank_row,
+                      rank_row_token, cap, status);
+}
+
+cudaError_t launch_expand(const void* rank_buf, const int32_t* rank_offsets, int R, int64_t cap,
+                          const int32_t* rank_row_token, const int32_t* pair_rank_row,
+                          const int32_t* dst_row, int64_t T, int64_t H, int k, void* recv,
+                          int64_t rows, uint32_t* status, cudaStream_t stream) {
+    if (cap == 0 || T == 0) return cudaSuccess;
+    return launch_pdl(expand_kernel, dim3(blocks_for(cap, kWarps)), dim3(kWarps * 32), 0, stream,
+                      static_cast<const uint4*>(rank_buf), rank_offsets, R, cap, rank_row_token,
+                      pair_rank_row, dst_row, T, H / 8, k, static_cast<uint4*>(recv), rows, status);
+}
+
+cudaError_t launch_combine_partial(const void* y, int64_t rows, const float* topk_w,
+                                   const int32_t* dst_row, const int32_t* pair_rank_row,
+                                   const int32_t* rank_row_token, const int32_t* rank_offsets,
+                                   int R, int64_t cap, int64_t T, int64_t H, int k, void* partial,
+                                   uint32_t* status, cudaStream_t stream) {
+    if (cap == 0 || T == 0) return cudaSuccess;
+    return launch_pdl(combine_partial_kernel, dim3(blocks_for(cap, kWarps)), dim3(kWarps * 32), 0,
+                      stream, static_cast<const uint4*>(y), rows, topk_w, dst_row, pair_rank_row,
+                      rank_row_token, rank_offsets, R, cap, T, H / 8, k,
+                      static_cast<uint4*>(partial), status);
+}
+
+cudaError_t launch_combine_reduce(const void* partial, int64_t cap, const int32_t* rank_dst_row,
+                                  int64_t T, int64_t H, int k, void* out, uint32_t* status,
+                                  cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    return launch_pdl(combine_reduce_kernel, dim3(blocks_for(T, kWarps)), dim3(kWarps * 32), 0,
+                      stream, static_cast<const uint4*>(partial), cap, rank_dst_row, T, H / 8, k,
+                      static_cast<uint4*>(out), status);
+}
+
+}  // namespace ep

@@ -230,6 +230,70 @@ EP_API int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row
                uint32_t* status, void* stream);
 
 /*
+ * Two-stage (rank, then expert) form of dispatch and combine -- the shape of
+ * the pages' transport: one copy of a token per virtual rank it reaches,
+ * expanded on arrival into that rank's experts (dispatch_copy_epilogue in the
+ * afdEP kernel traces; PR #1238's review: one copy per destination node, then
+ * forwarding to the local experts), and on the way back a rank-local partial
+ * reduction followed by the final reduction over the token's ranks
+ * (combine_reduce_epilogue).  With ranks being regions of one GPU, the copy to
+ * ranks is ep_dispatch(x, .., rank_dst_row, rank_buf, rank_rows, ..).
+ *
+ * ep_rank_layout: every (token t, rank r) that t reaches gets one row of a
+ * rank buffer; rank r owns rows [rank_offsets[r], rank_offsets[r+1]), in
+ * token order.
+ *  rank_counts      [R] out: tokens reaching rank r.
+ *  rank_offsets     [R+1] out: exclusive scan; rank_offsets[R] = rows used
+ *                   (at most T * min(k, R): size rank buffers for that).
+ *  rank_dst_row     [T,k] out: the rank row for the FIRST pair of each
+ *                   (token, rank), -1 for the token's other pairs in that rank
+ *                   and for pairs without a valid expert.
+ *  pair_rank_row    [T,k] out: the rank row of every pair with a valid expert.
+ *  rank_row_token   [rank_rows] out: the token of each rank row; rank_rows
+ *                   should be T * min(k, R) (rows beyond it are not written
+ *                   and raise EP_FLAG_BAD_ROW).
+ *  workspace        ep_rank_layout_workspace_bytes(T, k, E, R) bytes,
+ *                   16-byte aligned, no initialisation needed.
+ *  status           zeroed, then EP_FLAG_BAD_EXPERT for ids outside [-1, E).
+ */
+EP_API size_t ep_rank_layout_workspace_bytes(int64_t T, int k, int E, int R);
+EP_API int ep_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                          int32_t* rank_counts, int32_t* rank_offsets, int32_t* rank_dst_row,
+                          int32_t* pair_rank_row, int32_t* rank_row_token, int64_t rank_rows,
+                          uint32_t* status, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
+ * ep_expand: recv[dst_row[t,j]] = rank_buf[pair_rank_row[t,j]] for every pair
+ * (bit copy), one pass over each rank row.  rank_buf is [rank_rows, H] bf16
+ * (rank_rows = its allocated rows, >= rank_offsets[R]); the kernels read the
+ * live row count from rank_offsets[R] on the device.
+ */
+EP_API int ep_expand(const void* rank_buf, const int32_t* rank_offsets, int R, int64_t rank_rows,
+                     const int32_t* rank_row_token, const int32_t* pair_rank_row,
+                     const int32_t* dst_row, int64_t T, int64_t H, int k, void* recv,
+                     int64_t rows, uint32_t* status, void* stream);
+
+/*
+ * ep_combine_partial: for each rank row i of token t,
+ *   partial[i] = bf16_rne( fp32 FMA chain, increasing j, over the pairs of t
+ *                with pair_rank_row == i and dst_row != -1, of
+ *                topk_w[t,j] * y[dst_row[t,j]] ).
+ * ep_combine_reduce: out[t] = bf16_rne( fp32 sum, increasing j, of
+ *   partial[rank_dst_row[t,j]] over the pairs with rank_dst_row != -1 ).
+ * The two together equal ep_combine up to the extra bf16 rounding of each
+ * partial (|difference| <= 2^-9 * sum_r |partial_r| + one final rounding).
+ */
+EP_API int ep_combine_partial(const void* y, int64_t rows, const float* topk_w,
+                              const int32_t* dst_row, const int32_t* pair_rank_row,
+                              const int32_t* rank_row_token, const int32_t* rank_offsets, int R,
+                              int64_t rank_rows, int64_t T, int64_t H, int k, void* partial,
+                              uint32_t* status, void* stream);
+EP_API int ep_combine_reduce(const void* partial, int64_t rank_rows, const int32_t* rank_dst_row,
+                             int64_t T, int64_t H, int k, void* out, uint32_t* status,
+                             void* stream);
+
+/*
  * Host-buffer executor.  ep_roundtrip_host() runs one whole step -- route to
  * the device, ep_layout, ep_dispatch, ep_combine, result back -- for inputs and
  * output in pinned HOST memory, overlapping the copies with the kernels in

@@ -121,3 +121,17 @@ def test_aligned_layout_argument_validation(lib):
     assert call(T=1 << 27, k=8, E=1024, R=1, align=1 << 21) == 1   # padded rows >= 2^31
     assert call(E=255) == 1
     assert call(ws=None) == 3
+
+
+def test_two_stage_argument_validation(lib):
+    assert lib.ep_rank_layout_workspace_bytes(0, 8, 256, 16) == 0
+    assert lib.ep_rank_layout_workspace_bytes(65536, 8, 256, 16) >= 65536 * 8 * 4
+    assert lib.ep_rank_layout(FAKE, 16, 8, 255, 16, FAKE, FAKE, FAKE, FAKE, FAKE, 128, None, FAKE,
+                              1 << 30, None) == 1   # E % R
+    assert lib.ep_rank_layout(FAKE, 16, 8, 256, 16, FAKE, FAKE, FAKE, FAKE, FAKE, 128, None, None,
+                              0, None) == 3         # workspace
+    assert lib.ep_expand(FAKE, FAKE, 0, 10, FAKE, FAKE, FAKE, 4, 64, 8, FAKE, 32, None, None) == 1
+    assert lib.ep_expand(FAKE, FAKE, 4, 10, FAKE, FAKE, FAKE, 4, 60, 8, FAKE, 32, None, None) == 2
+    assert lib.ep_combine_partial(FAKE, 32, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 4, 64, 8, None,
+                                  None, None) == 1  # partial NULL
+    assert lib.ep_combine_reduce(FAKE, 10, FAKE, 4, 64, 8, None, None, None) == 1
