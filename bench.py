@@ -62,6 +62,9 @@ def parse():
                     help="budget of the timed oracle sample (cpu_baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", default="direct", choices=["direct", "two_stage"],
+                    help="direct: layout, dispatch, combine; two_stage: one copy per (token, rank), "
+                         "expansion into experts, rank-local partial combine, final reduce")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step as one captured CUDA graph (launch-bound small shapes)")
     return ap.parse_args()
@@ -318,7 +321,35 @@ def run_ours(args, rank, world, local):
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    if args.path == "two_stage":
+        if wl.payload != "bf16":
+            raise SystemExit("the two-stage path is BF16 only")
+        cap = ep.rank_rows_bound(wl.T, wl.k, wl.R)
+        rl = ep.rank_layout(idx, wl.E, wl.R)
+        rank_buf = torch.empty(cap, wl.H, dtype=torch.bfloat16, device=dev)
+        partial = torch.empty(cap, wl.H, dtype=torch.bfloat16, device=dev)
+        rws = torch.empty(max(16, ep.load().ep_rank_layout_workspace_bytes(wl.T, wl.k, wl.E, wl.R)),
+                          dtype=torch.uint8, device=dev)
+
+    def step_two_stage(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
+        ep.rank_layout(idx, wl.E, wl.R, out=rl, workspace=rws)
+        if ev:
+            ev[1].record(stream)
+        ep.dispatch(x, rl.rank_dst_row, cap, recv=rank_buf, status=lay.status)
+        ep.expand(rank_buf, rl, lay.dst_row, wl.rows, recv=recv, status=lay.status)
+        if ev:
+            ev[2].record(stream)
+        ep.combine_partial(y, w, lay.dst_row, rl, cap, partial=partial, status=lay.status)
+        ep.combine_reduce(partial, rl, wl.T, out=out, status=lay.status)
+        if ev:
+            ev[3].record(stream)
+
     def step(ev=None):
+        if args.path == "two_stage":
+            return step_two_stage(ev)
         if ev:
             ev[0].record(stream)
         ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
@@ -335,8 +366,13 @@ def run_ours(args, rank, world, local):
         if ev:
             ev[3].record(stream)
 
-    # launches of our kernels per step: 3 layout kernels + dispatch + combine
-    launches_per_step = 5
+    # launches of our kernels per step: 3 layout kernels (1 when T <= 2048) +
+    # dispatch + combine; the two-stage path adds the rank layout (keys, the
+    # layout over keys, finish), the expansion and the final reduce
+    lay_launches = 1 if wl.T <= 2048 else 3
+    launches_per_step = lay_launches + 2
+    if args.path == "two_stage":
+        launches_per_step = 2 * lay_launches + 2 + 4
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -421,7 +457,7 @@ def run_ours(args, rank, world, local):
     # layout, streams x in token chunks overlapped with dispatch + combine, and
     # streams the output back, all inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.path == "direct":
         xh = x.cpu().pin_memory()
         ih = idx.cpu().pin_memory()
         wh = w.cpu().pin_memory()
@@ -477,7 +513,8 @@ def run_ours(args, rank, world, local):
                        "l2": "inputs larger than L2 (x %.2f GB, dispatch buffer %.2f GB); no flush"
                              % (x.numel() * 2 / 1e9, wl.rows * wl.H * (1 if wl.payload == 'fp8' else 2) / 1e9),
                        "parallelism": "replicas x%d" % world,
-                       "launch": "cuda graph" if args.graph else "stream (programmatic dependent launch)"},
+                       "launch": "cuda graph" if args.graph else "stream (programmatic dependent launch)",
+                       "path": args.path},
             "roofline": roofline,
             "kernels": kernels,
             "cpu_baseline": cpu,
