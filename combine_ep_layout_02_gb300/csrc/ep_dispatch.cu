@@ -19,6 +19,14 @@
 #ifndef EP_DISPATCH_U
 #define EP_DISPATCH_U 4  // 16-byte vectors per lane in flight per row pass
 #endif
+#ifndef EP_FP8_MIN_BLOCKS
+#define EP_FP8_MIN_BLOCKS 0  // >0: resident blocks per SM the FP8 kernel is compiled for
+#endif
+#if EP_FP8_MIN_BLOCKS > 0
+#define EP_FP8_BOUNDS __launch_bounds__(256, EP_FP8_MIN_BLOCKS)
+#else
+#define EP_FP8_BOUNDS __launch_bounds__(256)
+#endif
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
 #endif
@@ -93,7 +101,8 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
 // FP8: each lane owns 16 consecutive channels (two 16-byte loads, one
 // 16-byte store of codes per destination row); 8 lanes form one 128-channel
 // block; a warp covers 512 channels per iteration.
-__global__ void __launch_bounds__(kDispatchWarps * 32)
+static_assert(kDispatchWarps * 32 == 256, "EP_FP8_BOUNDS assumes 256-thread blocks");
+__global__ void EP_FP8_BOUNDS
 dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
                     const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv_q,
                     float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status) {

@@ -345,21 +345,23 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     }
 }
 
-// Small batches (T <= kFusedMaxTokens): the whole layout in one block of
-// 1024 threads.  Warp w owns tokens [w*tpw, (w+1)*tpw) (tpw a multiple of
-// 32); per-warp shared histograms give, after an exclusive scan over the
-// warps, each warp's base slot per expert, and the block scan over experts
-// gives the offsets -- the same stable slots as the chunked kernels, in one
-// launch.
-constexpr int kFusedThreads = 1024;
-constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr int kFusedMaxTokens = 2048;
+// Small batches (T <= kFusedMaxTokens): the whole layout in one block of NT
+// threads (NT/32 warps of 32 tokens each).  Warp w owns tokens
+// [w*tpw, (w+1)*tpw); per-warp shared histograms give, after an exclusive scan
+// over the warps, each warp's base slot per expert, and the block scan over
+// experts gives the offsets -- the same stable slots as the chunked kernels,
+// in one launch.  One SM does all the work, so larger batches use the
+// chunked kernels, which spread it over the GPU.
+constexpr int kFusedMaxTokens = 512;
 
-__global__ void __launch_bounds__(kFusedThreads)
+template <int NT>
+__global__ void __launch_bounds__(NT)
 layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
                     int capacity, int align, int tpw, int32_t* __restrict__ expert_counts,
                     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
                     int32_t* __restrict__ rank_token_counts, uint32_t* __restrict__ status) {
+    constexpr int kFusedThreads = NT;
+    constexpr int kFusedWarps = NT / 32;
     extern __shared__ __align__(16) int32_t smem_i[];
     const int npad = kFusedWarps * tpw * k;
     int32_t* s_idx = smem_i;                    // [npad]
@@ -382,13 +384,17 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     __syncthreads();
 
     const int wp0 = warp * tpw * k;
-    const int npieces = tpw * k / 32;
+    const int active_warps = (T + tpw - 1) / tpw;  // warps that own at least one token
+    const bool active = warp < active_warps;       // warp-uniform
+    // pieces holding this warp's pairs (the last active warp may have fewer)
+    const int wpairs = active ? min(tpw * k, T * k - wp0) : 0;
+    const int npieces = (wpairs + 31) / 32;
     int32_t* my_w = s_w + warp * E;
     for (int m = 0; m < npieces; ++m) {
         const int e = s_idx[wp0 + m * 32 + lane];
         if (e >= 0 && e < E) atomicAdd(&my_w[e], 1);
     }
-    if (R_cols > 0)
+    if (R_cols > 0 && active)
         for (int i = 0; i < tpw; i += 32) {
             const int t = warp * tpw + i + lane;
             if (t < T) count_token_ranks(s_idx + t * k, k, E, R_cols, s_rank_of, s_rank);
@@ -396,7 +402,7 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kFusedThreads) {
         int run = 0;
-        for (int w = 0; w < kFusedWarps; ++w) {
+        for (int w = 0; w < active_warps; ++w) {
             const int v = s_w[w * E + e];
             s_w[w * E + e] = run;
             run += v;
@@ -464,13 +470,25 @@ size_t assign_smem_bytes(int k, int E) {
            sizeof(int32_t);
 }
 
-size_t fused_smem_bytes(int tpw, int k, int E, int R_cols) {
-    return ((size_t)kFusedWarps * tpw * k + (size_t)kFusedWarps * E + 3 * (size_t)E + 1 + R_cols +
-            kFusedWarps) *
+size_t fused_smem_bytes(int warps, int tpw, int k, int E, int R_cols) {
+    return ((size_t)warps * tpw * k + (size_t)warps * E + 3 * (size_t)E + 1 + R_cols + warps) *
            sizeof(int32_t);
 }
 
 constexpr size_t kFusedSmemLimit = 160 * 1024;
+
+template <int NT>
+cudaError_t launch_fused(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols, int kind,
+                         int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
+                         int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
+                         size_t smem, cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(layout_fused_kernel<NT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(layout_fused_kernel<NT>, dim3(1), dim3(NT), smem, stream, topk_idx, (int)T,
+                      k, E, R_cols, kind, capacity, align, 32, expert_counts, expert_offsets,
+                      dst_row, rank_token_counts, status);
+}
 
 }  // namespace
 
@@ -483,16 +501,17 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                           expert_offsets, rank_token_counts, status);
     const int R_cols = rank_token_counts ? R : 0;
     if (T <= kFusedMaxTokens) {
-        const int tpw = 32 * (int)((T + 32 * kFusedWarps - 1) / (32 * kFusedWarps));
-        const size_t smem = fused_smem_bytes(tpw, k, E, R_cols);
+        // one warp per 32 tokens: 128 threads up to 128 tokens, else 512
+        const int nt = T <= 128 ? 128 : 512;
+        const size_t smem = fused_smem_bytes(nt / 32, 32, k, E, R_cols);
         if (smem <= kFusedSmemLimit) {
-            cudaError_t err = cudaFuncSetAttribute(
-                layout_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (err != cudaSuccess) return err;
-            return launch_pdl(layout_fused_kernel, dim3(1), dim3(kFusedThreads), smem, stream,
-                              topk_idx, (int)T, k, E, R_cols, kind, capacity, align, tpw,
-                              expert_counts,
-                              expert_offsets, dst_row, rank_token_counts, status);
+            if (nt == 128)
+                return launch_fused<128>(topk_idx, T, k, E, R_cols, kind, capacity, align,
+                                         expert_counts, expert_offsets, dst_row,
+                                         rank_token_counts, status, smem, stream);
+            return launch_fused<512>(topk_idx, T, k, E, R_cols, kind, capacity, align,
+                                     expert_counts, expert_offsets, dst_row, rank_token_counts,
+                                     status, smem, stream);
         }
     }
     const int64_t nchunk = layout_num_chunks(T);
