@@ -104,6 +104,35 @@ def aggregate_value(logical_bytes_per_step, steps, max_seconds, world):
     return world * logical_bytes_per_step * steps / max_seconds / 1e9
 
 
+def provenance(dev, idx, w, x):
+    """Versions, git revision and input hashes recorded with every result."""
+    info = {"torch": torch.__version__, "cuda": torch.version.cuda,
+            "device": torch.cuda.get_device_name(dev)}
+    try:
+        info["git"] = subprocess.run(["git", "rev-parse", "--short", "HEAD"], cwd=ROOT,
+                                     capture_output=True, text=True, timeout=10).stdout.strip() or None
+    except (OSError, subprocess.TimeoutExpired):
+        info["git"] = None
+    try:
+        info["driver"] = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                                        capture_output=True, text=True, timeout=10).stdout.split()[0]
+    except (OSError, subprocess.TimeoutExpired, IndexError):
+        info["driver"] = None
+    try:
+        info["nvcc"] = subprocess.run(["nvcc", "--version"], capture_output=True, text=True,
+                                      timeout=10).stdout.strip().splitlines()[-1]
+    except (OSError, subprocess.TimeoutExpired, IndexError):
+        info["nvcc"] = None
+    try:  # digest of the CUDA sources and flags the library was built from
+        with open(os.path.join(ROOT, "combine_ep_layout_02_gb300", "_build", "stamp")) as f:
+            info["library_source_digest"] = f.read().strip()[:16]
+    except OSError:
+        info["library_source_digest"] = None
+    info["sha256_route_weights"] = W.sha256_of(idx, w)
+    info["sha256_x_first_64MB"] = W.sha256_of(x.view(-1)[: (64 << 20) // 2])
+    return info
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -522,7 +551,7 @@ def run_ours(args, rank, world, local):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "device": props.name,
-            "versions": {"torch": torch.__version__, "cuda": torch.version.cuda},
+            "provenance": provenance(dev, idx, w, x),
         }
         print(json.dumps(line), flush=True)
 

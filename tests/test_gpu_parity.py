@@ -372,3 +372,38 @@ def test_layout_reused_across_calls():
         used = rows_of(ref["dst_row"])
         assert np.array_equal(_bits(recv)[used], rrecv[used])
         assert np.array_equal(_bits(out), oracle.combine_fp32_seq(rrecv, w.cpu().numpy(), ref["dst_row"]))
+
+
+# --------------------------------------------------------------------------- large top-k (k > 8)
+
+@pytest.mark.parametrize("k,E,H", [(9, 64, 1024), (16, 256, 7168), (32, 1024, 512)])
+def test_large_topk_paths(k, E, H):
+    # k > 8 takes the generic paths (row pointers in passes of 8, combine
+    # batches of 8 rows inside each column group)
+    T = 300
+    rng = np.random.default_rng(k * 7 + E)
+    keys = rng.random((T, E))
+    idx = np.argsort(-keys, axis=1)[:, :k].astype(np.int32)   # k distinct experts per token
+    idx[5, 3] = -1                                              # one unrouted pair
+    idx_d = torch.from_numpy(idx).to(DEV)
+    lay = ep.layout(idx_d, E, 4, "contiguous")
+    ref = _compare_layout(idx, E, 4, "contiguous", 0, lay, expect_flags=0)
+    rows = T * k
+    x = torch.randn(T, H, device=DEV).to(torch.bfloat16)
+    recv = ep.dispatch(x, lay.dst_row, rows, status=lay.status)
+    rrecv = oracle.dispatch_bf16(_bits(x), ref["dst_row"], rows)
+    used = rows_of(ref["dst_row"])
+    assert np.array_equal(_bits(recv)[used], rrecv[used])
+    if H % 128 == 0:
+        q, s = ep.dispatch_fp8(x, lay.dst_row, rows, status=lay.status)
+        rq, rs = oracle.dispatch_fp8(_bits(x), ref["dst_row"], rows)
+        assert np.array_equal(q.cpu().numpy()[used], rq[used])
+        assert np.array_equal(s.cpu().numpy()[used].view(np.uint32), rs[used].view(np.uint32))
+    w = torch.rand(T, k, device=DEV)
+    y = torch.randn(rows, H, device=DEV).to(torch.bfloat16)
+    out = ep.combine(y, w, lay.dst_row, status=lay.status)
+    assert ep.status_read(lay.status) == 0
+    yb = _bits(y)
+    assert np.array_equal(_bits(out), oracle.combine_fp32_seq(yb, w.cpu().numpy(), ref["dst_row"]))
+    _, r64, absum = oracle.combine_f64(yb, w.cpu().numpy(), ref["dst_row"])
+    check_combine(_bits(out), r64, absum, "k=%d" % k)
