@@ -27,6 +27,9 @@
 #else
 #define EP_FP8_BOUNDS __launch_bounds__(256)
 #endif
+#ifndef EP_FP8_U
+#define EP_FP8_U 2  // 512-channel groups per FP8 iteration (loads issued together)
+#endif
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
 #endif
@@ -100,12 +103,50 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
 
 // FP8: each lane owns 16 consecutive channels (two 16-byte loads, one
 // 16-byte store of codes per destination row); 8 lanes form one 128-channel
-// block; a warp covers 512 channels per iteration.
+// block; a warp covers 512 channels per group and EP_FP8_U groups per
+// iteration (their loads are issued together).
+struct Fp8Group {
+    uint4 q;   // 16 e4m3 codes of this lane
+    float sf;  // scale of this lane's 128-channel block
+};
+
+__device__ __forceinline__ Fp8Group quantize16(const uint4& a, const uint4& b) {
+    const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16lo_to_f32(wv[i]);
+        f[2 * i + 1] = bf16hi_to_f32(wv[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+    const float ap = fmaxf(amax, 1e-4f);
+    Fp8Group g;
+    g.sf = __fdiv_rn(ap, 448.0f);
+    const float inv = __fdiv_rn(448.0f, ap);
+    uint32_t qw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo =
+            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
+        const uint32_t hi =
+            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
+        qw[i] = lo | (hi << 16);
+    }
+    g.q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    return g;
+}
+
 static_assert(kDispatchWarps * 32 == 256, "EP_FP8_BOUNDS assumes 256-thread blocks");
 __global__ void EP_FP8_BOUNDS
 dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
                     const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv_q,
                     float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status) {
+    constexpr int U = EP_FP8_U;
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -121,47 +162,31 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
             const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
             rr[jj] = (j0 + jj < k) ? r : -1;
         }
-        for (int64_t c0 = 0; c0 < H; c0 += 512) {
-            const int64_t c = c0 + lane * 16;
-            const bool act = c < H;  // H % 128 == 0: all 8 lanes of a block agree
-            uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-            if (act) {
-                a = ld_stream_v4(src + c);
-                b = ld_stream_v4(src + c + 8);
+        for (int64_t c0 = 0; c0 < H; c0 += 512 * U) {
+            uint4 a[U], b[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + u * 512 + lane * 16;
+                a[u] = make_uint4(0, 0, 0, 0);
+                b[u] = make_uint4(0, 0, 0, 0);
+                if (c < H) {  // H % 128 == 0: all 8 lanes of a block agree
+                    a[u] = ld_stream_v4(src + c);
+                    b[u] = ld_stream_v4(src + c + 8);
+                }
             }
-            const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float f[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                f[2 * i] = bf16lo_to_f32(wv[i]);
-                f[2 * i + 1] = bf16hi_to_f32(wv[i]);
-            }
-            float amax = 0.0f;
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + u * 512 + lane * 16;
+                const bool act = c < H;
+                const Fp8Group g = quantize16(a[u], b[u]);
+                const bool scale_writer = act && (lane & 7) == 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-            const float ap = fmaxf(amax, 1e-4f);
-            const float sf = __fdiv_rn(ap, 448.0f);
-            const float inv = __fdiv_rn(448.0f, ap);
-            uint32_t qw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t lo =
-                    cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
-                const uint32_t hi =
-                    cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
-                qw[i] = lo | (hi << 16);
-            }
-            const uint4 q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-            const bool scale_writer = act && (lane & 7) == 0;
-#pragma unroll
-            for (int jj = 0; jj < kRowRegs; ++jj) {
-                const int r = rr[jj];
-                if (r < 0) continue;  // warp-uniform
-                if (act) st_v4(recv_q + (int64_t)r * H + c, q);
-                if (scale_writer) recv_scale[(int64_t)r * nblk + (c >> 7)] = sf;
+                for (int jj = 0; jj < kRowRegs; ++jj) {
+                    const int r = rr[jj];
+                    if (r < 0) continue;  // warp-uniform
+                    if (act) st_v4(recv_q + (int64_t)r * H + c, g.q);
+                    if (scale_writer) recv_scale[(int64_t)r * nblk + (c >> 7)] = g.sf;
+                }
             }
         }
     }
