@@ -537,7 +537,7 @@ def run_ours(args, rank, world, local):
             "vs_baseline": None, "dtype": wl.payload, "data": "synthetic",
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "k": wl.k,
                        "R": wl.R, "layout": wl.kind, "payload": wl.payload, "route": wl.route,
-                       "zipf_s": wl.zipf_s, "expert_outputs": wl.expert_out,
+                       "zipf_s": wl.zipf_s, "expert_outputs": wl.expert_out, "seed": wl.seed,
                        "logical_bytes_per_step": logical,
                        "l2": "inputs larger than L2 (x %.2f GB, dispatch buffer %.2f GB); no flush"
                              % (x.numel() * 2 / 1e9, wl.rows * wl.H * (1 if wl.payload == 'fp8' else 2) / 1e9),

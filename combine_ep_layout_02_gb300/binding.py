@@ -60,6 +60,7 @@ def load():
         "ep_rank_layout_workspace_bytes": ([i64, i32, i32, i32], sz),
         "ep_rank_layout": ([P, i64, i32, i32, i32, P, P, P, P, P, i64, P, P, sz, P], i32),
         "ep_expand": ([P, P, i32, i64, P, P, P, i64, i64, i32, P, i64, P, P], i32),
+        "ep_expand_fp8": ([P, P, P, i32, i64, P, P, P, i64, i64, i32, P, P, i64, P, P], i32),
         "ep_combine_partial": ([P, i64, P, P, P, P, P, i32, i64, i64, i64, i32, P, P, P], i32),
         "ep_combine_reduce": ([P, i64, P, i64, i64, i32, P, P, P], i32),
         "ep_dispatch_fp8": ([P, i64, i64, i32, P, P, P, i64, P, P], i32),
@@ -273,6 +274,25 @@ def expand(rank_buf, rl, dst_row, rows, recv=None, status=None):
                             k, _ptr(recv), rows, _ptr(status), _stream(rank_buf.device))
     _rc("ep_expand", code)
     return recv
+
+
+def expand_fp8(rank_q, rank_scale, rl, dst_row, rows, recv_q=None, recv_scale=None, status=None):
+    """Expansion of FP8 rank rows (codes and scales) into the expert rows (see ``ep_expand_fp8``)."""
+    _check_dev("rank_q", rank_q, torch.uint8)
+    _check_dev("rank_scale", rank_scale, torch.float32)
+    T, k = dst_row.shape
+    H = rank_q.shape[1]
+    R = rl.rank_counts.numel()
+    if recv_q is None:
+        recv_q = torch.empty(rows, H, dtype=torch.uint8, device=rank_q.device)
+    if recv_scale is None:
+        recv_scale = torch.empty(rows, H // 128, dtype=torch.float32, device=rank_q.device)
+    code = load().ep_expand_fp8(_ptr(rank_q), _ptr(rank_scale), _ptr(rl.rank_offsets), R,
+                                rank_q.shape[0], _ptr(rl.rank_row_token), _ptr(rl.pair_rank_row),
+                                _ptr(dst_row), T, H, k, _ptr(recv_q), _ptr(recv_scale), rows,
+                                _ptr(status), _stream(rank_q.device))
+    _rc("ep_expand_fp8", code)
+    return recv_q, recv_scale
 
 
 def combine_partial(y, topk_w, dst_row, rl, rank_rows, partial=None, status=None):

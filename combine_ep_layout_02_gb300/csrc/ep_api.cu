@@ -199,6 +199,28 @@ int ep_expand(const void* rank_buf, const int32_t* rank_offsets, int R, int64_t 
                                          as_stream(stream)));
 }
 
+int ep_expand_fp8(const uint8_t* rank_q, const float* rank_scale, const int32_t* rank_offsets,
+                  int R, int64_t rank_rows, const int32_t* rank_row_token,
+                  const int32_t* pair_rank_row, const int32_t* dst_row, int64_t T, int64_t H,
+                  int k, uint8_t* recv_q, float* recv_scale, int64_t rows, uint32_t* status,
+                  void* stream) {
+    int rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (H % 128 != 0) return EP_ERR_ALIGNMENT;
+    if (R < 1 || rank_rows < 0 || rank_rows > (int64_t)INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (T == 0 || rank_rows == 0) return EP_OK;
+    if (!rank_q || !rank_scale || !rank_offsets || !rank_row_token || !pair_rank_row ||
+        !dst_row || ((!recv_q || !recv_scale) && rows > 0))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(rank_q, 16) || !aligned(recv_q, 16) || !aligned(rank_scale, 4) ||
+        !aligned(recv_scale, 4) || !aligned(rank_offsets, 4) || !aligned(rank_row_token, 4) ||
+        !aligned(pair_rank_row, 4) || !aligned(dst_row, 4) || !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(ep::launch_expand_fp8(rank_q, rank_scale, rank_offsets, R, rank_rows,
+                                             rank_row_token, pair_rank_row, dst_row, T, H, k,
+                                             recv_q, recv_scale, rows, status, as_stream(stream)));
+}
+
 int ep_combine_partial(const void* y, int64_t rows, const float* topk_w, const int32_t* dst_row,
                        const int32_t* pair_rank_row, const int32_t* rank_row_token,
                        const int32_t* rank_offsets, int R, int64_t rank_rows, int64_t T,

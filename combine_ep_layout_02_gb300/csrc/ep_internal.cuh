@@ -226,6 +226,12 @@ cudaError_t launch_expand(const void* rank_buf, const int32_t* rank_offsets, int
                           const int32_t* rank_row_token, const int32_t* pair_rank_row,
                           const int32_t* dst_row, int64_t T, int64_t H, int k, void* recv,
                           int64_t rows, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_expand_fp8(const uint8_t* rank_q, const float* rank_scale,
+                              const int32_t* rank_offsets, int R, int64_t cap,
+                              const int32_t* rank_row_token, const int32_t* pair_rank_row,
+                              const int32_t* dst_row, int64_t T, int64_t H, int k,
+                              uint8_t* recv_q, float* recv_scale, int64_t rows, uint32_t* status,
+                              cudaStream_t stream);
 cudaError_t launch_combine_partial(const void* y, int64_t rows, const float* topk_w,
                                    const int32_t* dst_row, const int32_t* pair_rank_row,
                                    const int32_t* rank_row_token, const int32_t* rank_offsets,

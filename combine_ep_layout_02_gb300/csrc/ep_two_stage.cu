@@ -12,7 +12,8 @@
 //                 -> finish kernel (pair_rank_row for every pair, the token
 //                 of every rank row).
 //   expand      : one warp per rank row, copying it to the expert rows of its
-//                 token's pairs in that rank.
+//                 token's pairs in that rank (BF16 rows, or FP8 code rows plus
+//                 their fp32 scale rows).
 //   partial     : one warp per rank row, fp32 FMA chain over those pairs in
 //                 increasing j, rounded to bf16.
 //   reduce      : one warp per token, fp32 sum of its rank rows' partials in
@@ -126,12 +127,57 @@ __device__ __forceinline__ int64_t live_rank_rows(const int32_t* rank_offsets, i
     return n;
 }
 
+// Copy of a rank row to the expert rows of its token's pairs in that rank.
+// Rows are `nvec` vectors of type V (16-byte uint4 for bf16 rows and e4m3
+// codes, 4-byte words for fp32 scale rows).
+template <typename V>
+__device__ __forceinline__ V ld_row_vec(const V* p);
+template <>
+__device__ __forceinline__ uint4 ld_row_vec<uint4>(const uint4* p) { return ld_stream_v4(p); }
+template <>
+__device__ __forceinline__ uint32_t ld_row_vec<uint32_t>(const uint32_t* p) { return __ldg(p); }
+
+template <typename V>
+__device__ __forceinline__ void expand_row(const V* __restrict__ src, V* __restrict__ dst_base,
+                                           int64_t nvec, int k, int my_row, int lane) {
+    constexpr int U = 4;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        V* dst[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
+            dst[jj] = (j0 + jj < k && r >= 0) ? dst_base + (int64_t)r * nvec : nullptr;
+        }
+        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+            V buf[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * 32 + lane;
+                if (v < nvec) buf[u] = ld_row_vec<V>(src + v);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                if (dst[jj] == nullptr) continue;  // warp-uniform
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = v0 + u * 32 + lane;
+                    if (v < nvec) dst[jj][v] = buf[u];
+                }
+            }
+        }
+    }
+}
+
+// One warp per rank row: copies rank row i of up to two arrays (the payload
+// rows a, and optionally the scale rows b) to the expert rows of its pairs.
+template <typename VA, typename VB>
 __global__ void __launch_bounds__(kWarps * 32)
-expand_kernel(const uint4* __restrict__ rank_buf, const int32_t* __restrict__ rank_offsets, int R,
-              int64_t cap, const int32_t* __restrict__ rank_row_token,
+expand_kernel(const VA* __restrict__ a_src, VA* __restrict__ a_dst, int64_t a_nvec,
+              const VB* __restrict__ b_src, VB* __restrict__ b_dst, int64_t b_nvec,
+              const int32_t* __restrict__ rank_offsets, int R, int64_t cap,
+              const int32_t* __restrict__ rank_row_token,
               const int32_t* __restrict__ pair_rank_row, const int32_t* __restrict__ dst_row,
-              int64_t T, int64_t nvec, int k, uint4* __restrict__ recv, int64_t rows,
-              uint32_t* __restrict__ status) {
+              int64_t T, int k, int64_t rows, uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -143,33 +189,8 @@ expand_kernel(const uint4* __restrict__ rank_buf, const int32_t* __restrict__ ra
         return;
     }
     const int my_row = rank_row_pair(i, t, k, pair_rank_row, dst_row, rows, status);
-    const uint4* src = rank_buf + i * nvec;
-    constexpr int U = 4;
-    for (int j0 = 0; j0 < k; j0 += 8) {
-        uint4* dst[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
-            dst[jj] = (j0 + jj < k && r >= 0) ? recv + (int64_t)r * nvec : nullptr;
-        }
-        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
-            uint4 buf[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * 32 + lane;
-                if (v < nvec) buf[u] = ld_stream_v4(src + v);
-            }
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                if (dst[jj] == nullptr) continue;  // warp-uniform
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int64_t v = v0 + u * 32 + lane;
-                    if (v < nvec) st_v4(dst[jj] + v, buf[u]);
-                }
-            }
-        }
-    }
+    expand_row<VA>(a_src + i * a_nvec, a_dst, a_nvec, k, my_row, lane);
+    if (b_src != nullptr) expand_row<VB>(b_src + i * b_nvec, b_dst, b_nvec, k, my_row, lane);
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
@@ -328,9 +349,26 @@ cudaError_t launch_expand(const void* rank_buf, const int32_t* rank_offsets, int
                           const int32_t* dst_row, int64_t T, int64_t H, int k, void* recv,
                           int64_t rows, uint32_t* status, cudaStream_t stream) {
     if (cap == 0 || T == 0) return cudaSuccess;
-    return launch_pdl(expand_kernel, dim3(blocks_for(cap, kWarps)), dim3(kWarps * 32), 0, stream,
-                      static_cast<const uint4*>(rank_buf), rank_offsets, R, cap, rank_row_token,
-                      pair_rank_row, dst_row, T, H / 8, k, static_cast<uint4*>(recv), rows, status);
+    return launch_pdl(expand_kernel<uint4, uint4>, dim3(blocks_for(cap, kWarps)),
+                      dim3(kWarps * 32), 0, stream, static_cast<const uint4*>(rank_buf),
+                      static_cast<uint4*>(recv), H / 8, (const uint4*)nullptr, (uint4*)nullptr,
+                      (int64_t)0, rank_offsets, R, cap, rank_row_token, pair_rank_row, dst_row, T,
+                      k, rows, status);
+}
+
+cudaError_t launch_expand_fp8(const uint8_t* rank_q, const float* rank_scale,
+                              const int32_t* rank_offsets, int R, int64_t cap,
+                              const int32_t* rank_row_token, const int32_t* pair_rank_row,
+                              const int32_t* dst_row, int64_t T, int64_t H, int k,
+                              uint8_t* recv_q, float* recv_scale, int64_t rows, uint32_t* status,
+                              cudaStream_t stream) {
+    if (cap == 0 || T == 0) return cudaSuccess;
+    return launch_pdl(expand_kernel<uint4, uint32_t>, dim3(blocks_for(cap, kWarps)),
+                      dim3(kWarps * 32), 0, stream, reinterpret_cast<const uint4*>(rank_q),
+                      reinterpret_cast<uint4*>(recv_q), H / 16,
+                      reinterpret_cast<const uint32_t*>(rank_scale),
+                      reinterpret_cast<uint32_t*>(recv_scale), H / 128, rank_offsets, R, cap,
+                      rank_row_token, pair_rank_row, dst_row, T, k, rows, status);
 }
 
 cudaError_t launch_combine_partial(const void* y, int64_t rows, const float* topk_w,

@@ -275,6 +275,18 @@ EP_API int ep_expand(const void* rank_buf, const int32_t* rank_offsets, int R, i
                      int64_t rows, uint32_t* status, void* stream);
 
 /*
+ * ep_expand_fp8: the same for an FP8 rank buffer (the copy to ranks being
+ * ep_dispatch_fp8(x, .., rank_dst_row, rank_q, rank_scale, rank_rows, ..)):
+ * codes [rank_rows, H] and scales [rank_rows, H/128] of each rank row are
+ * copied to recv_q / recv_scale rows dst_row[t,j].  H % 128 == 0.
+ */
+EP_API int ep_expand_fp8(const uint8_t* rank_q, const float* rank_scale,
+                         const int32_t* rank_offsets, int R, int64_t rank_rows,
+                         const int32_t* rank_row_token, const int32_t* pair_rank_row,
+                         const int32_t* dst_row, int64_t T, int64_t H, int k, uint8_t* recv_q,
+                         float* recv_scale, int64_t rows, uint32_t* status, void* stream);
+
+/*
  * ep_combine_partial: for each rank row i of token t,
  *   partial[i] = bf16_rne( fp32 FMA chain, increasing j, over the pairs of t
  *                with pair_rank_row == i and dst_row != -1, of

@@ -135,3 +135,12 @@ def test_two_stage_argument_validation(lib):
     assert lib.ep_combine_partial(FAKE, 32, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 4, 64, 8, None,
                                   None, None) == 1  # partial NULL
     assert lib.ep_combine_reduce(FAKE, 10, FAKE, 4, 64, 8, None, None, None) == 1
+
+
+def test_expand_fp8_argument_validation(lib):
+    assert lib.ep_expand_fp8(FAKE, FAKE, FAKE, 4, 10, FAKE, FAKE, FAKE, 4, 64, 8, FAKE, FAKE, 32,
+                             None, None) == 2       # H % 128
+    assert lib.ep_expand_fp8(FAKE, FAKE, FAKE, 0, 10, FAKE, FAKE, FAKE, 4, 128, 8, FAKE, FAKE, 32,
+                             None, None) == 1       # R < 1
+    assert lib.ep_expand_fp8(None, FAKE, FAKE, 4, 10, FAKE, FAKE, FAKE, 4, 128, 8, FAKE, FAKE, 32,
+                             None, None) == 1

@@ -102,3 +102,28 @@ def test_two_stage_full_size_prefill():
         assert torch.equal(ri[d[c0:c0 + (1 << 16)]], xi[tok[c0:c0 + (1 << 16)]])
     # one copy per (token, rank) reached
     assert int(rl.rank_offsets[-1]) == int(lay.rank_token_counts.sum())
+
+
+@pytest.mark.parametrize("name,T,H", [("decode_fp8", 2048, 7168), ("prefill_fp8", 1500, 384)])
+def test_two_stage_fp8_matches_direct_and_oracle(name, T, H):
+    wl = W.WORKLOADS[name].scaled(T=T, H=H, capacity=min(W.WORKLOADS[name].capacity, T) or None)
+    x = W.hidden_states(wl, device=DEV)
+    idx = W.route(wl, device=DEV)
+    lay = ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity)
+    rl = ep.rank_layout(idx, wl.E, wl.R)
+    cap = ep.rank_rows_bound(wl.T, wl.k, wl.R)
+    rq, rs = ep.dispatch_fp8(x, rl.rank_dst_row, cap)          # one quantised copy per (token, rank)
+    q2, s2 = ep.expand_fp8(rq, rs, rl, lay.dst_row, wl.rows, status=lay.status)
+    q1, s1 = ep.dispatch_fp8(x, lay.dst_row, wl.rows, status=lay.status)
+    assert ep.status_read(lay.status) == 0
+    used = lay.dst_row.view(-1).long()
+    assert torch.equal(q2[used], q1[used])
+    assert torch.equal(s2[used].view(torch.int32), s1[used].view(torch.int32))
+    dst = lay.dst_row.cpu().numpy()
+    keep = dst.reshape(-1) >= 0
+    compact = np.full(dst.size, -1, np.int32)
+    compact[keep] = np.arange(int(keep.sum()), dtype=np.int32)
+    oq, os_ = oracle.dispatch_fp8(_bits(x), compact.reshape(dst.shape), int(keep.sum()))
+    rows_used = torch.from_numpy(dst.reshape(-1)[keep].astype(np.int64)).to(DEV)
+    assert np.array_equal(q2[rows_used].cpu().numpy(), oq)
+    assert np.array_equal(s2[rows_used].cpu().numpy().view(np.uint32), os_.view(np.uint32))
