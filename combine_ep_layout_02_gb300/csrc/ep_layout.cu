@@ -28,6 +28,8 @@
 // Masked layouts use the same slots with row = e * capacity + slot.  With an
 // expert alignment m > 1 (contiguous only) each expert's segment is padded to
 // a multiple of m rows: the offsets scan ceil(count / m) * m instead.
+#include <atomic>
+
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -482,9 +484,20 @@ cudaError_t launch_fused(const int32_t* topk_idx, int64_t T, int k, int E, int R
                          int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
                          int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
                          size_t smem, cudaStream_t stream) {
-    cudaError_t err = cudaFuncSetAttribute(layout_fused_kernel<NT>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // raise the kernel's shared-memory limit once per device (to the largest
+    // size this path ever requests)
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        err = cudaFuncSetAttribute(layout_fused_kernel<NT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kFusedSmemLimit);
+        if (err != cudaSuccess) return err;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
     return launch_pdl(layout_fused_kernel<NT>, dim3(1), dim3(NT), smem, stream, topk_idx, (int)T,
                       k, E, R_cols, kind, capacity, align, 32, expert_counts, expert_offsets,
                       dst_row, rank_token_counts, status);
