@@ -5,7 +5,9 @@ Default workload: the Prefill-like shape (65,536 tokens = 16 virtual ranks x
 layout, BF16 dispatch and combine; combine runs over the dispatched rows,
 i.e. identity experts).  Inputs are generated on the device before timing
 and are far larger than L2 (x 0.94 GB, dispatch buffer 7.5 GB), so no L2
-flush is inserted between steps.
+flush is inserted between steps.  Workloads whose working set is under four
+times the L2 size get a 2 x L2 buffer written between steps, outside the
+timed events (one event pair per step).
 
 Prints ONE JSON line (rank 0).  `value` is the logical throughput: the
 useful payload of one dispatch plus one combine (each (token, expert)
@@ -65,6 +67,10 @@ def parse():
     ap.add_argument("--path", default="direct", choices=["direct", "two_stage"],
                     help="direct: layout, dispatch, combine; two_stage: one copy per (token, rank), "
                          "expansion into experts, rank-local partial combine, final reduce")
+    ap.add_argument("--l2-flush", action="store_true",
+                    help="flush L2 between steps even when the working set is far larger than L2")
+    ap.add_argument("--no-l2-flush", action="store_true",
+                    help="never flush L2 (warm-L2 numbers for working sets that fit in L2)")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step as one captured CUDA graph (launch-bound small shapes)")
     return ap.parse_args()
@@ -417,27 +423,58 @@ def run_ours(args, rank, world, local):
     if ep.status_read(lay.status) != 0:
         raise SystemExit("device status flags set during warm-up")
 
+    # L2 policy: the working set of a step must exceed L2 by a wide margin,
+    # else L2 is flushed (a buffer twice its size is written) between steps
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
+    elem = 1 if wl.payload == "fp8" else 2
+    touched = (x.numel() * 2 + wl.T * wl.k * wl.H * elem + wl.T * wl.k * wl.H * 2
+               + out.numel() * 2)
+    flush = args.l2_flush or (touched < 4 * l2_bytes and not args.no_l2_flush)
+    if flush:
+        flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+        l2_note = ("L2 flushed between steps (%d MB written outside the timed events); "
+                   "working set %.0f MB" % (flush_buf.numel() >> 20, touched / 1e6))
+    elif touched < 4 * l2_bytes:
+        l2_note = "warm L2 (no flush requested); working set %.0f MB" % (touched / 1e6)
+    else:
+        l2_note = ("inputs larger than L2 (x %.2f GB, dispatch buffer %.2f GB, working set %.1f GB); "
+                   "no flush" % (x.numel() * 2 / 1e9, wl.rows * wl.H * elem / 1e9, touched / 1e9))
+
     # timed region: K steps between one event pair, nothing else on the stream
-    # (so consecutive kernels keep their programmatic-dependent-launch overlap)
+    # (so consecutive kernels keep their programmatic-dependent-launch overlap);
+    # with an L2 flush, one event pair per step and the flush outside it
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(local)
     time.sleep(0.3)  # let the sampler start
-    t_start.record(stream)
-    for _ in range(args.steps):
-        run_step()
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
+    if flush:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            pairs[i][0].record(stream)
+            run_step()
+            pairs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = sum(a.elapsed_time(b) for a, b in pairs)
+    else:
+        t_start.record(stream)
+        for _ in range(args.steps):
+            run_step()
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = t_start.elapsed_time(t_end)
     clocks = sampler.stop()
     barrier(world, dev)
-    total_ms = t_start.elapsed_time(t_end)
 
     # per-kernel times: the same K steps again with an event pair around each
     # call (events between kernels, so no launch overlap at those boundaries)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(i & 0xFF)
         step(evs[i])
     torch.cuda.synchronize(dev)
     lay_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
@@ -539,8 +576,7 @@ def run_ours(args, rank, world, local):
                        "R": wl.R, "layout": wl.kind, "payload": wl.payload, "route": wl.route,
                        "zipf_s": wl.zipf_s, "expert_outputs": wl.expert_out, "seed": wl.seed,
                        "logical_bytes_per_step": logical,
-                       "l2": "inputs larger than L2 (x %.2f GB, dispatch buffer %.2f GB); no flush"
-                             % (x.numel() * 2 / 1e9, wl.rows * wl.H * (1 if wl.payload == 'fp8' else 2) / 1e9),
+                       "l2": l2_note,
                        "parallelism": "replicas x%d" % world,
                        "launch": "cuda graph" if args.graph else "stream (programmatic dependent launch)",
                        "path": args.path},
