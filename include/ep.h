@@ -15,7 +15,9 @@
  *
  * Conventions for every call
  *  - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
- *    (allocates and frees) every buffer; the library allocates nothing.
+ *    (allocates and frees) every buffer; the library allocates no device
+ *    memory (ep_layout_static_ws uses one fixed array of the library's own;
+ *    ep_pipeline_create makes streams and events, no memory).
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Every call only enqueues work on `stream` and returns; nothing
  *    synchronises except ep_status_read().
@@ -70,7 +72,8 @@ enum {
     EP_FLAG_BAD_EXPERT = 1u, /* an expert id outside [-1, E): the pair was skipped */
     EP_FLAG_OVERFLOW = 2u,   /* masked layout: slot >= capacity, the pair was dropped */
     EP_FLAG_BAD_ROW = 4u,    /* dispatch/combine: dst_row outside [-1, rows): skipped */
-    EP_FLAG_TIMEOUT = 8u     /* a bounded wait for an in-flight copy gave up: output incomplete */
+    EP_FLAG_TIMEOUT = 8u     /* a bounded wait for an in-flight copy gave up: output
+                                incomplete (only the optional bulk-copy dispatch build waits) */
 };
 
 typedef enum { EP_LAYOUT_CONTIGUOUS = 0, EP_LAYOUT_MASKED = 1 } ep_layout_kind_t;
