@@ -2,7 +2,9 @@
 // scan and stable slot assignment (the "dispatch layout" that the Prefill-like
 // profile of awsome-distributed-ai PR #1238 times inside its boundary).
 //
-// Three small kernels chained with programmatic dependent launch; no block
+// Batches of up to 512 tokens use one single-block kernel, up to 2048 tokens
+// one 8-block cluster kernel (both further down); larger batches use three
+// small kernels chained with programmatic dependent launch, where no block
 // ever waits on another block:
 //   1. count  : one 128-thread block per chunk of 128 tokens.  The chunk's
 //               ids are staged in shared memory with one coalesced pass, then
@@ -28,6 +30,8 @@
 // Masked layouts use the same slots with row = e * capacity + slot.  With an
 // expert alignment m > 1 (contiguous only) each expert's segment is padded to
 // a multiple of m rows: the offsets scan ceil(count / m) * m instead.
+#include <cooperative_groups.h>
+
 #include <atomic>
 
 #include "ep_internal.cuh"
@@ -448,6 +452,134 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     }
 }
 
+// Medium batches (T <= kClusterMaxTokens): the whole layout in ONE launch of
+// one 8-block thread-block cluster.  Each block owns 256 tokens (a warp per
+// 32) and builds its per-warp expert histograms; after a cluster barrier
+// every block reads the 8 block histograms through distributed shared memory
+// (the blocks before it give its base slots, all of them the totals), and a
+// second cluster barrier keeps every block resident until all remote reads
+// are done.  The barriers are hardware cluster barriers: no block ever spins
+// on memory.
+namespace cg = cooperative_groups;
+constexpr int kClusterBlocks = 8;
+constexpr int kClusterThreads = 256;
+constexpr int kClusterWarps = kClusterThreads / 32;
+constexpr int kClusterTokens = kClusterThreads;  // tokens per block
+constexpr int kClusterMaxTokens = kClusterBlocks * kClusterTokens;
+
+__global__ void __launch_bounds__(kClusterThreads)
+layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
+                      int capacity, int align, int32_t* __restrict__ expert_counts,
+                      int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
+                      int32_t* __restrict__ rank_token_counts, uint32_t* __restrict__ status) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int b = (int)cluster.block_rank();
+    extern __shared__ __align__(16) int32_t smem_i[];
+    const int npad = kClusterTokens * k;
+    int32_t* s_idx = smem_i;                      // [npad]
+    int32_t* s_w = s_idx + npad;                  // [kClusterWarps][E]
+    int32_t* s_hist = s_w + kClusterWarps * E;    // [E + R_cols]  block totals (read remotely)
+    int32_t* s_tot = s_hist + E + R_cols;         // [E]
+    int32_t* s_base = s_tot + E;                  // [E]
+    int32_t* s_off = s_base + E;                  // [E + 1]
+    int32_t* s_rank_of = s_off + E + 1;           // [E]
+    int32_t* s_rank = s_rank_of + E;              // [R_cols]
+    int32_t* s_warp = s_rank + R_cols;            // [kClusterWarps]
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int t0 = b * kClusterTokens;
+    const int ntok = T - t0 < 0 ? 0 : (T - t0 < kClusterTokens ? T - t0 : kClusterTokens);
+
+    pdl_wait();
+    pdl_trigger();
+    if (b == 0 && threadIdx.x == 0 && status) *status = 0u;
+    stage_ids(idx, (int64_t)t0 * k, ntok * k, npad, s_idx);
+    for (int i = threadIdx.x; i < kClusterWarps * E; i += kClusterThreads) s_w[i] = 0;
+    for (int i = threadIdx.x; i < R_cols; i += kClusterThreads) s_rank[i] = 0;
+    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
+    __syncthreads();
+
+    const int wp0 = warp * 32 * k;
+    const int wtok = ntok - warp * 32;                           // tokens of this warp
+    const int npieces = wtok <= 0 ? 0 : ((wtok < 32 ? wtok : 32) * k + 31) / 32;
+    int32_t* my_w = s_w + warp * E;
+    for (int m = 0; m < npieces; ++m) {
+        const int e = s_idx[wp0 + m * 32 + lane];
+        if (e >= 0 && e < E) atomicAdd(&my_w[e], 1);
+    }
+    if (R_cols > 0 && threadIdx.x < ntok)
+        count_token_ranks(s_idx + threadIdx.x * k, k, E, R_cols, s_rank_of, s_rank);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kClusterThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kClusterWarps; ++w) {
+            const int v = s_w[w * E + e];
+            s_w[w * E + e] = run;
+            run += v;
+        }
+        s_hist[e] = run;
+    }
+    for (int r = threadIdx.x; r < R_cols; r += kClusterThreads) s_hist[E + r] = s_rank[r];
+    cluster.sync();  // every block's histogram is complete and visible
+
+    for (int e = threadIdx.x; e < E; e += kClusterThreads) {
+        int before = 0, total = 0;
+#pragma unroll
+        for (int q = 0; q < kClusterBlocks; ++q) {
+            const int v = cluster.map_shared_rank(s_hist, q)[e];
+            before += q < b ? v : 0;
+            total += v;
+        }
+        s_base[e] = before;
+        s_tot[e] = (total + align - 1) / align * align;  // padded segment length
+        if (b == 0) expert_counts[e] = total;
+    }
+    if (b == 0 && rank_token_counts)
+        for (int r = threadIdx.x; r < R_cols; r += kClusterThreads) {
+            int total = 0;
+#pragma unroll
+            for (int q = 0; q < kClusterBlocks; ++q) total += cluster.map_shared_rank(s_hist, q)[E + r];
+            rank_token_counts[r] = total;
+        }
+    cluster.sync();  // no block leaves while another still reads its histogram
+
+    block_exclusive_scan<kClusterThreads>(s_tot, E, s_off, s_warp);
+    if (b == 0)
+        for (int e = threadIdx.x; e <= E; e += kClusterThreads) expert_offsets[e] = s_off[e];
+
+    const unsigned lt = lanemask_lt();
+    const int key_bits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);
+    const int npairs = ntok * k;
+    int32_t* out = dst_row + (int64_t)t0 * k;
+    for (int m = 0; m < npieces; ++m) {
+        const int lp = wp0 + m * 32 + lane;
+        const bool in_range = lp < npairs;
+        const int e = s_idx[lp];
+        const bool valid = (e >= 0) && (e < E);
+        const bool bad = in_range && !valid && e != -1;
+        const unsigned peers = warp_peers(valid, e, key_bits);
+        bool overflow = false;
+        int dst = -1;
+        if (valid) {
+            const int slot = s_base[e] + my_w[e] + __popc(peers & lt);
+            if (kind == EP_LAYOUT_CONTIGUOUS) {
+                dst = s_off[e] + slot;
+            } else if (slot < capacity) {
+                dst = e * capacity + slot;
+            } else {
+                overflow = true;
+            }
+        }
+        if (in_range) out[lp] = dst;
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) my_w[e] += __popc(peers);
+        __syncwarp();
+        warp_flag(status, bad, EP_FLAG_BAD_EXPERT);
+        warp_flag(status, overflow, EP_FLAG_OVERFLOW);
+    }
+}
+
 // T == 0: write the (all-zero) outputs so that callers always get defined data.
 __global__ void layout_empty_kernel(int E, int R, int32_t* expert_counts,
                                     int32_t* expert_offsets, int32_t* rank_token_counts,
@@ -503,6 +635,47 @@ cudaError_t launch_fused(const int32_t* topk_idx, int64_t T, int k, int E, int R
                       dst_row, rank_token_counts, status);
 }
 
+size_t cluster_smem_bytes(int k, int E, int R_cols) {
+    return ((size_t)kClusterTokens * k + (size_t)kClusterWarps * E + (E + R_cols) + 3 * (size_t)E +
+            1 + E + R_cols + kClusterWarps) *
+           sizeof(int32_t);
+}
+
+cudaError_t launch_cluster(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols, int kind,
+                           int capacity, int align, int32_t* expert_counts,
+                           int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
+                           uint32_t* status, size_t smem, cudaStream_t stream) {
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        err = cudaFuncSetAttribute(layout_cluster_kernel,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kFusedSmemLimit);
+        if (err != cudaSuccess) return err;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterBlocks);
+    cfg.blockDim = dim3(kClusterThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterBlocks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, topk_idx, (int)T, k, E, R_cols, kind,
+                              capacity, align, expert_counts, expert_offsets, dst_row,
+                              rank_token_counts, status);
+}
+
 }  // namespace
 
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
@@ -526,6 +699,13 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                                      expert_counts, expert_offsets, dst_row, rank_token_counts,
                                      status, smem, stream);
         }
+    }
+    if (T <= kClusterMaxTokens) {
+        const size_t smem = cluster_smem_bytes(k, E, R_cols);
+        if (smem <= kFusedSmemLimit)
+            return launch_cluster(topk_idx, T, k, E, R_cols, kind, capacity, align, expert_counts,
+                                  expert_offsets, dst_row, rank_token_counts, status, smem,
+                                  stream);
     }
     const int64_t nchunk = layout_num_chunks(T);
     const int ncol = E + R_cols;
