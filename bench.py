@@ -401,10 +401,10 @@ def run_ours(args, rank, world, local):
         if ev:
             ev[3].record(stream)
 
-    # launches of our kernels per step: 3 layout kernels (1 when T <= 512) +
+    # launches of our kernels per step: 3 layout kernels (1 when T <= 2048) +
     # dispatch + combine; the two-stage path adds the rank layout (keys, the
     # layout over keys, finish), the expansion and the final reduce
-    lay_launches = 1 if wl.T <= 512 else 3  # fused single-block layout up to 512 tokens
+    lay_launches = 1 if wl.T <= 2048 else 3  # one launch (single block or one cluster) up to 2048 tokens
     launches_per_step = lay_launches + 2
     if args.path == "two_stage":
         launches_per_step = 2 * lay_launches + 2 + 4
