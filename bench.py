@@ -71,6 +71,8 @@ def parse():
                     help="flush L2 between steps even when the working set is far larger than L2")
     ap.add_argument("--no-l2-flush", action="store_true",
                     help="never flush L2 (warm-L2 numbers for working sets that fit in L2)")
+    ap.add_argument("--layout-only", action="store_true",
+                    help="time only the routing layout (20 calls captured in one CUDA graph)")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step as one captured CUDA graph (launch-bound small shapes)")
     return ap.parse_args()
@@ -310,6 +312,52 @@ def run_reference(args, rank, world):
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def run_layout_only(args, rank, world, local):
+    """The routing layout alone: `--steps` replays of a CUDA graph holding 20
+    layout calls on the workload's route (a few MB on the device)."""
+    import combine_ep_layout_02_gb300 as ep
+    if not os.path.exists(ep.binding.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.scaled(T=args.tokens, capacity=min(wl.capacity, args.tokens) or None)
+    idx = W.route(wl, device=dev)
+    lay = ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity)
+    ws = torch.empty(max(16, ep.layout_workspace_bytes(wl.T, wl.k, wl.E, wl.R)), dtype=torch.uint8,
+                     device=dev)
+    for _ in range(max(3, args.warmup)):
+        ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
+    torch.cuda.synchronize(dev)
+    calls = 20
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(calls):
+            ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize(dev)
+    if ep.status_read(lay.status) != 0:
+        raise SystemExit("device status flags set by the layout")
+    us = a.elapsed_time(b) * 1e3 / (args.steps * calls)
+    pairs = wl.T * wl.k
+    if rank == 0:
+        print(json.dumps({"metric": "routing layout us per call (CUDA graph of %d calls)" % calls,
+                          "value": us, "unit": "us", "higher_is_better": False, "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup,
+                          "config": {"workload": wl.name, "T": wl.T, "k": wl.k, "E": wl.E,
+                                     "R": wl.R, "layout": wl.kind},
+                          "pairs_per_us": pairs / us,
+                          "launches_per_call": 1 if wl.T <= 2048 else 3}), flush=True)
 
 
 def run_ours(args, rank, world, local):
@@ -598,6 +646,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.layout_only:
+            run_layout_only(args, rank, world, local)
         else:
             run_ours(args, rank, world, local)
     finally:

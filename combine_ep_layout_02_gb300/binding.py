@@ -400,3 +400,19 @@ class Pipeline:
             self.close()
         except Exception:
             pass
+
+
+# The C ABI's names, for callers who prefer them (same functions as above).
+ep_layout = layout
+ep_layout_aligned = layout  # alignment= selects ep_layout_aligned
+ep_layout_static_ws = layout_static_ws
+ep_dispatch = dispatch
+ep_dispatch_fp8 = dispatch_fp8
+ep_combine = combine
+ep_rank_layout = rank_layout
+ep_expand = expand
+ep_expand_fp8 = expand_fp8
+ep_combine_partial = combine_partial
+ep_combine_reduce = combine_reduce
+ep_status_read = status_read
+ep_layout_workspace_bytes = layout_workspace_bytes
