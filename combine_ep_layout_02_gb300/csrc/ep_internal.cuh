@@ -29,6 +29,27 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return v;
 }
 
+// 32-byte streaming load (sm_100+ 256-bit vector access); `p` 32-byte aligned.
+struct Vec32 {
+    uint4 lo, hi;
+};
+__device__ __forceinline__ Vec32 ld_stream_v8(const void* p) {
+    Vec32 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x),
+                   "=r"(v.hi.y), "=r"(v.hi.z), "=r"(v.hi.w)
+                 : "l"(p));
+    return v;
+}
+
+// 32-byte store; `p` 32-byte aligned.
+__device__ __forceinline__ void st_v8(void* p, const Vec32& v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v.lo.x),
+                 "r"(v.lo.y), "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x), "r"(v.hi.y), "r"(v.hi.z),
+                 "r"(v.hi.w)
+                 : "memory");
+}
+
 // 16-byte store.
 __device__ __forceinline__ void st_v4(void* p, const uint4& v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),

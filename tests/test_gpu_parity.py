@@ -407,3 +407,36 @@ def test_large_topk_paths(k, E, H):
     assert np.array_equal(_bits(out), oracle.combine_fp32_seq(yb, w.cpu().numpy(), ref["dst_row"]))
     _, r64, absum = oracle.combine_f64(yb, w.cpu().numpy(), ref["dst_row"])
     check_combine(_bits(out), r64, absum, "k=%d" % k)
+
+
+# --------------------------------------------------------------------------- 32-byte combine path
+
+@pytest.mark.parametrize("T,k,H,offset", [(17000, 8, 528, 0), (20000, 16, 1024, 0), (16384, 8, 256, 16)])
+def test_combine_large_batch_paths(T, k, H, offset):
+    # T >= 16384 with H % 16 == 0 and 32-byte-aligned buffers takes the
+    # 32-byte-access kernel (k > 8: its batched path); a 16-byte offset on the
+    # output falls back to the 16-byte kernel.  Results are the same FMA chain.
+    E = 64
+    rng = np.random.default_rng(T + k)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    idx[7, 1] = -1
+    lay = ep.layout(torch.from_numpy(idx).to(DEV), E, 4, "contiguous")
+    rows = T * k
+    y = torch.randn(rows, H, device=DEV).to(torch.bfloat16)
+    w = torch.rand(T, k, device=DEV)
+    raw = torch.empty(T * H + offset // 2 + 16, dtype=torch.bfloat16, device=DEV)
+    out = raw[offset // 2: offset // 2 + T * H].view(T, H)
+    ep.combine(y, w, lay.dst_row, out=out, status=lay.status)
+    assert ep.status_read(lay.status) == 0
+    rng2 = np.random.default_rng(0)
+    ts = np.concatenate([[0, 7, T - 1], rng2.choice(T, 200, replace=False)])
+    dst = lay.dst_row.cpu().numpy()[ts]
+    keep = dst >= 0
+    compact = np.where(keep, np.arange(dst.size, dtype=np.int32).reshape(dst.shape), -1).astype(np.int32)
+    gather = torch.from_numpy(np.where(keep, dst, 0).reshape(-1).astype(np.int64)).to(DEV)
+    yb = _bits(y[gather])
+    wb = w.cpu().numpy()[ts]
+    got = _bits(out[torch.from_numpy(ts).to(DEV)])
+    assert np.array_equal(got, oracle.combine_fp32_seq(yb, wb, compact))
+    _, r64, absum = oracle.combine_f64(yb, wb, compact)
+    check_combine(got, r64, absum, "T=%d k=%d" % (T, k))
