@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="prefill", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=None,
+                    help="override the workload's seed (inputs are drawn from it)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="scale the workload to this many tokens (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=30)
@@ -371,6 +373,8 @@ def run_ours(args, rank, world, local):
     wl = W.WORKLOADS[args.workload]
     if args.tokens:
         wl = wl.scaled(T=args.tokens, capacity=min(wl.capacity, args.tokens) or None)
+    if args.seed is not None:
+        wl = wl.scaled(seed=args.seed)
     torch.manual_seed(0)
 
     # ---- inputs resident in HBM

@@ -30,6 +30,9 @@
 #ifndef EP_FP8_U
 #define EP_FP8_U 2  // 512-channel groups per FP8 iteration (loads issued together)
 #endif
+#ifndef EP_FP8_LOAD32
+#define EP_FP8_LOAD32 0  // 1: one 32-byte load per lane and group instead of two 16-byte loads
+#endif
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
 #endif
@@ -170,8 +173,14 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
                 a[u] = make_uint4(0, 0, 0, 0);
                 b[u] = make_uint4(0, 0, 0, 0);
                 if (c < H) {  // H % 128 == 0: all 8 lanes of a block agree
+#if EP_FP8_LOAD32
+                    const Vec32 v = ld_stream_v8(src + c);  // 32-byte aligned: H % 128 == 0
+                    a[u] = v.lo;
+                    b[u] = v.hi;
+#else
                     a[u] = ld_stream_v4(src + c);
                     b[u] = ld_stream_v4(src + c + 8);
+#endif
                 }
             }
 #pragma unroll
