@@ -29,6 +29,12 @@
  *    bits into the optional `status` word (a device uint32), which the caller
  *    reads with ep_status_read().  ep_layout() zeroes the word first;
  *    ep_dispatch*() and ep_combine() only OR into it.
+ *  - Kernels are launched with programmatic stream serialisation: each one
+ *    waits for the preceding work in the stream before touching memory, and
+ *    lets the next kernel launch early.  A caller's own kernel launched right
+ *    after one of ours WITH that launch attribute must wait on the grid
+ *    dependency (griddepcontrol.wait / cudaGridDependencySynchronize) before
+ *    reading our outputs; ordinary launches, copies and events need nothing.
  *  - bf16 tensors are passed as raw 16-bit patterns, row-major.
  *  - dst_row[t*k + j] is the row of the dispatch buffer that receives token t
  *    for its j-th expert, or -1 when the pair is not routed (expert id -1, a
