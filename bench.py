@@ -41,7 +41,7 @@ METRIC = "dispatch+combine logical GB/s per call (layout+dispatch+combine, one e
 KERNEL_SOURCES = {
     "layout": "combine_ep_layout_02_gb300/csrc/ep_layout.cu",
     "dispatch": "combine_ep_layout_02_gb300/csrc/ep_dispatch.cu",
-    "dispatch_fp8": "combine_ep_layout_02_gb300/csrc/ep_dispatch.cu",
+    "dispatch_fp8": "combine_ep_layout_02_gb300/csrc/ep_dispatch_fp8.cu",
     "combine": "combine_ep_layout_02_gb300/csrc/ep_combine.cu",
 }
 

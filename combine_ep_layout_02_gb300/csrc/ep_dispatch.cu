@@ -1,13 +1,10 @@
-// ep_dispatch.cu -- dispatch (scatter of token rows into the per-expert
-// buffer), BF16 bit copy and the fused per-token FP8 e4m3 cast.
+// ep_dispatch.cu -- BF16 dispatch: scatter of token rows into the
+// per-expert buffer (bit copy).  The FP8 variant is in ep_dispatch_fp8.cu.
 //
 // One warp per token.  The warp reads the token row once in 16-byte vectors
 // (streaming, no L1 allocation) and writes it to each of its k destination
 // rows, so every input byte is read once and every output byte written once:
-// the HBM floor is T*H*2 read + T*k*H*2 (BF16) or T*k*(H + H/32) (FP8) written.
-// The FP8 variant computes the block amax with three xor-shuffles over the 8
-// lanes that share a 128-channel block, so the cast costs no extra pass over
-// memory (PR #1238 measures the unfused cast as a separate launch-bound step).
+// the HBM floor is T*H*2 read + T*k*H*2 written.
 #include "ep_internal.cuh"
 
 #ifndef EP_DISPATCH_BULK
@@ -19,20 +16,6 @@
 #ifndef EP_DISPATCH_U
 #define EP_DISPATCH_U 4  // 16-byte vectors per lane in flight per row pass
 #endif
-#ifndef EP_FP8_MIN_BLOCKS
-#define EP_FP8_MIN_BLOCKS 0  // >0: resident blocks per SM the FP8 kernel is compiled for
-#endif
-#if EP_FP8_MIN_BLOCKS > 0
-#define EP_FP8_BOUNDS __launch_bounds__(256, EP_FP8_MIN_BLOCKS)
-#else
-#define EP_FP8_BOUNDS __launch_bounds__(256)
-#endif
-#ifndef EP_FP8_U
-#define EP_FP8_U 2  // 512-channel groups per FP8 iteration (loads issued together)
-#endif
-#ifndef EP_FP8_LOAD32
-#define EP_FP8_LOAD32 0  // 1: one 32-byte load per lane and group instead of two 16-byte loads
-#endif
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
 #endif
@@ -41,25 +24,7 @@ namespace ep {
 namespace {
 
 constexpr int kDispatchWarps = 8;  // warps (= tokens) per block
-
-// Row of pair (t, lane) for lane < k, validated against [-1, rows).
-__device__ __forceinline__ int load_dst_row(const int32_t* __restrict__ dst_row, int64_t t, int k,
-                                            int64_t rows, uint32_t* status) {
-    const int lane = threadIdx.x & 31;
-    int r = -1;
-    bool bad = false;
-    if (lane < k) {
-        r = __ldg(dst_row + t * k + lane);
-        if (r < -1 || (int64_t)r >= rows) {
-            bad = true;
-            r = -1;
-        }
-    }
-    warp_flag(status, bad, EP_FLAG_BAD_ROW);
-    return r;
-}
-
-constexpr int kRowRegs = 8;  // destination rows held in registers per pass
+constexpr int kRowRegs = 8;        // destination rows held in registers per pass
 
 template <int U>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
@@ -98,103 +63,6 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
                         if (EP_DISPATCH_STORE_CS) st_cs_v4(dst[jj] + v, buf[u]);
                         else st_v4(dst[jj] + v, buf[u]);
                     }
-                }
-            }
-        }
-    }
-}
-
-// FP8: each lane owns 16 consecutive channels (two 16-byte loads, one
-// 16-byte store of codes per destination row); 8 lanes form one 128-channel
-// block; a warp covers 512 channels per group and EP_FP8_U groups per
-// iteration (their loads are issued together).
-struct Fp8Group {
-    uint4 q;   // 16 e4m3 codes of this lane
-    float sf;  // scale of this lane's 128-channel block
-};
-
-__device__ __forceinline__ Fp8Group quantize16(const uint4& a, const uint4& b) {
-    const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float f[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        f[2 * i] = bf16lo_to_f32(wv[i]);
-        f[2 * i + 1] = bf16hi_to_f32(wv[i]);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-    const float ap = fmaxf(amax, 1e-4f);
-    Fp8Group g;
-    g.sf = __fdiv_rn(ap, 448.0f);
-    const float inv = __fdiv_rn(448.0f, ap);
-    uint32_t qw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t lo =
-            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
-        const uint32_t hi =
-            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
-        qw[i] = lo | (hi << 16);
-    }
-    g.q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-    return g;
-}
-
-static_assert(kDispatchWarps * 32 == 256, "EP_FP8_BOUNDS assumes 256-thread blocks");
-__global__ void EP_FP8_BOUNDS
-dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
-                    const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv_q,
-                    float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status) {
-    constexpr int U = EP_FP8_U;
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const int my_row = load_dst_row(dst_row, t, k, rows, status);
-    const int64_t nblk = H / 128;
-    const uint16_t* src = x + t * H;
-    for (int j0 = 0; j0 < k; j0 += kRowRegs) {
-        int rr[kRowRegs];
-#pragma unroll
-        for (int jj = 0; jj < kRowRegs; ++jj) {
-            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
-            rr[jj] = (j0 + jj < k) ? r : -1;
-        }
-        for (int64_t c0 = 0; c0 < H; c0 += 512 * U) {
-            uint4 a[U], b[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = c0 + u * 512 + lane * 16;
-                a[u] = make_uint4(0, 0, 0, 0);
-                b[u] = make_uint4(0, 0, 0, 0);
-                if (c < H) {  // H % 128 == 0: all 8 lanes of a block agree
-#if EP_FP8_LOAD32
-                    const Vec32 v = ld_stream_v8(src + c);  // 32-byte aligned: H % 128 == 0
-                    a[u] = v.lo;
-                    b[u] = v.hi;
-#else
-                    a[u] = ld_stream_v4(src + c);
-                    b[u] = ld_stream_v4(src + c + 8);
-#endif
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = c0 + u * 512 + lane * 16;
-                const bool act = c < H;
-                const Fp8Group g = quantize16(a[u], b[u]);
-                const bool scale_writer = act && (lane & 7) == 0;
-#pragma unroll
-                for (int jj = 0; jj < kRowRegs; ++jj) {
-                    const int r = rr[jj];
-                    if (r < 0) continue;  // warp-uniform
-                    if (act) st_v4(recv_q + (int64_t)r * H + c, g.q);
-                    if (scale_writer) recv_scale[(int64_t)r * nblk + (c >> 7)] = g.sf;
                 }
             }
         }
@@ -302,16 +170,6 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
     return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U>, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
                       static_cast<const uint4*>(x), T, nvec, k, dst_row, static_cast<uint4*>(recv),
                       rows, status);
-}
-
-cudaError_t launch_dispatch_fp8(const void* x, int64_t T, int64_t H, int k,
-                                const int32_t* dst_row, uint8_t* recv_q, float* recv_scale,
-                                int64_t rows, uint32_t* status, cudaStream_t stream) {
-    if (T == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
-    return launch_pdl(dispatch_fp8_kernel, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
-                      static_cast<const uint16_t*>(x), T, H, k, dst_row, recv_q, recv_scale, rows,
-                      status);
 }
 
 }  // namespace ep

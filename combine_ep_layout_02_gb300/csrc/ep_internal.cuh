@@ -186,6 +186,24 @@ __device__ __forceinline__ void warp_flag(uint32_t* status, bool cond, uint32_t 
     if (any && status && (threadIdx.x & 31) == 0) atomicOr(status, bit);
 }
 
+// Row of pair (t, lane) for lane < k, validated against [-1, rows): a row
+// outside raises EP_FLAG_BAD_ROW and the pair is skipped (-1).
+__device__ __forceinline__ int load_dst_row(const int32_t* __restrict__ dst_row, int64_t t, int k,
+                                            int64_t rows, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    int r = -1;
+    bool bad = false;
+    if (lane < k) {
+        r = __ldg(dst_row + t * k + lane);
+        if (r < -1 || (int64_t)r >= rows) {
+            bad = true;
+            r = -1;
+        }
+    }
+    warp_flag(status, bad, EP_FLAG_BAD_ROW);
+    return r;
+}
+
 // ---- launchers (host) ------------------------------------------------------
 
 // Record a CUDA error for ep_last_cuda_error() (host, per thread).
