@@ -98,6 +98,12 @@ def _check_dev(name, t, dtype, device=None):
         raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
 
 
+def _on(device):
+    """Run the enclosed C call with `device` current (the C ABI launches on the
+    current device)."""
+    return torch.cuda.device(device)
+
+
 def _rc(fn, code):
     if code != EP_OK:
         raise EpError(fn, code)
@@ -143,10 +149,11 @@ def layout(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=None, workspa
                                         _ptr(out.status), _ptr(workspace), wbytes, _stream(dev))
         _rc("ep_layout_aligned", code)
         return out
-    code = load().ep_layout(_ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity,
-                            _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.dst_row),
-                            _ptr(out.rank_token_counts), _ptr(out.status), _ptr(workspace), wbytes,
-                            _stream(dev))
+    with _on(dev):
+        code = load().ep_layout(_ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity,
+                                _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.dst_row),
+                                _ptr(out.rank_token_counts), _ptr(out.status), _ptr(workspace), wbytes,
+                                _stream(dev))
     _rc("ep_layout", code)
     return out
 
@@ -168,10 +175,11 @@ def layout_static_ws(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=Non
             torch.empty(R, dtype=torch.int32, device=dev) if with_rank_counts else None,
             torch.empty(1, dtype=torch.int32, device=dev),
         )
-    code = load().ep_layout_static_ws(_ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity,
-                                      _ptr(out.expert_counts), _ptr(out.expert_offsets),
-                                      _ptr(out.dst_row), _ptr(out.rank_token_counts),
-                                      _ptr(out.status), _stream(dev))
+    with _on(dev):
+        code = load().ep_layout_static_ws(_ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity,
+                                          _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                          _ptr(out.dst_row), _ptr(out.rank_token_counts),
+                                          _ptr(out.status), _stream(dev))
     _rc("ep_layout_static_ws", code)
     return out
 
@@ -185,8 +193,9 @@ def dispatch(x, dst_row, rows, recv=None, status=None):
     if recv is None:
         recv = torch.empty(rows, H, dtype=torch.bfloat16, device=x.device)
     _check_dev("recv", recv, torch.bfloat16, x.device)
-    code = load().ep_dispatch(_ptr(x), T, H, k, _ptr(dst_row), _ptr(recv), rows, _ptr(status),
-                              _stream(x.device))
+    with _on(x.device):
+        code = load().ep_dispatch(_ptr(x), T, H, k, _ptr(dst_row), _ptr(recv), rows, _ptr(status),
+                                  _stream(x.device))
     _rc("ep_dispatch", code)
     return recv
 
@@ -204,8 +213,9 @@ def dispatch_fp8(x, dst_row, rows, recv_q=None, recv_scale=None, status=None):
         recv_scale = torch.empty(rows, H // 128, dtype=torch.float32, device=x.device)
     _check_dev("recv_q", recv_q, torch.uint8, x.device)
     _check_dev("recv_scale", recv_scale, torch.float32, x.device)
-    code = load().ep_dispatch_fp8(_ptr(x), T, H, k, _ptr(dst_row), _ptr(recv_q), _ptr(recv_scale),
-                                  rows, _ptr(status), _stream(x.device))
+    with _on(x.device):
+        code = load().ep_dispatch_fp8(_ptr(x), T, H, k, _ptr(dst_row), _ptr(recv_q), _ptr(recv_scale),
+                                      rows, _ptr(status), _stream(x.device))
     _rc("ep_dispatch_fp8", code)
     return recv_q, recv_scale
 
@@ -220,8 +230,9 @@ def combine(y, topk_w, dst_row, out=None, status=None):
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=y.device)
     _check_dev("out", out, torch.bfloat16, y.device)
-    code = load().ep_combine(_ptr(y), _ptr(topk_w), _ptr(dst_row), T, H, k, rows, _ptr(out),
-                             _ptr(status), _stream(y.device))
+    with _on(y.device):
+        code = load().ep_combine(_ptr(y), _ptr(topk_w), _ptr(dst_row), T, H, k, rows, _ptr(out),
+                                 _ptr(status), _stream(y.device))
     _rc("ep_combine", code)
     return out
 
@@ -252,11 +263,12 @@ def rank_layout(topk_idx, E, R, *, out=None, workspace=None):
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     wbytes = workspace.numel() if workspace is not None else 0
-    code = load().ep_rank_layout(_ptr(topk_idx), T, k, E, R, _ptr(out.rank_counts),
-                                 _ptr(out.rank_offsets), _ptr(out.rank_dst_row),
-                                 _ptr(out.pair_rank_row), _ptr(out.rank_row_token),
-                                 out.rank_row_token.numel(), _ptr(out.status), _ptr(workspace),
-                                 wbytes, _stream(dev))
+    with _on(dev):
+        code = load().ep_rank_layout(_ptr(topk_idx), T, k, E, R, _ptr(out.rank_counts),
+                                     _ptr(out.rank_offsets), _ptr(out.rank_dst_row),
+                                     _ptr(out.pair_rank_row), _ptr(out.rank_row_token),
+                                     out.rank_row_token.numel(), _ptr(out.status), _ptr(workspace),
+                                     wbytes, _stream(dev))
     _rc("ep_rank_layout", code)
     return out
 
@@ -269,9 +281,10 @@ def expand(rank_buf, rl, dst_row, rows, recv=None, status=None):
     R = rl.rank_counts.numel()
     if recv is None:
         recv = torch.empty(rows, H, dtype=torch.bfloat16, device=rank_buf.device)
-    code = load().ep_expand(_ptr(rank_buf), _ptr(rl.rank_offsets), R, rank_buf.shape[0],
-                            _ptr(rl.rank_row_token), _ptr(rl.pair_rank_row), _ptr(dst_row), T, H,
-                            k, _ptr(recv), rows, _ptr(status), _stream(rank_buf.device))
+    with _on(rank_buf.device):
+        code = load().ep_expand(_ptr(rank_buf), _ptr(rl.rank_offsets), R, rank_buf.shape[0],
+                                _ptr(rl.rank_row_token), _ptr(rl.pair_rank_row), _ptr(dst_row), T, H,
+                                k, _ptr(recv), rows, _ptr(status), _stream(rank_buf.device))
     _rc("ep_expand", code)
     return recv
 
@@ -287,10 +300,11 @@ def expand_fp8(rank_q, rank_scale, rl, dst_row, rows, recv_q=None, recv_scale=No
         recv_q = torch.empty(rows, H, dtype=torch.uint8, device=rank_q.device)
     if recv_scale is None:
         recv_scale = torch.empty(rows, H // 128, dtype=torch.float32, device=rank_q.device)
-    code = load().ep_expand_fp8(_ptr(rank_q), _ptr(rank_scale), _ptr(rl.rank_offsets), R,
-                                rank_q.shape[0], _ptr(rl.rank_row_token), _ptr(rl.pair_rank_row),
-                                _ptr(dst_row), T, H, k, _ptr(recv_q), _ptr(recv_scale), rows,
-                                _ptr(status), _stream(rank_q.device))
+    with _on(rank_q.device):
+        code = load().ep_expand_fp8(_ptr(rank_q), _ptr(rank_scale), _ptr(rl.rank_offsets), R,
+                                    rank_q.shape[0], _ptr(rl.rank_row_token), _ptr(rl.pair_rank_row),
+                                    _ptr(dst_row), T, H, k, _ptr(recv_q), _ptr(recv_scale), rows,
+                                    _ptr(status), _stream(rank_q.device))
     _rc("ep_expand_fp8", code)
     return recv_q, recv_scale
 
@@ -303,10 +317,11 @@ def combine_partial(y, topk_w, dst_row, rl, rank_rows, partial=None, status=None
     R = rl.rank_counts.numel()
     if partial is None:
         partial = torch.empty(max(rank_rows, 1), H, dtype=torch.bfloat16, device=y.device)
-    code = load().ep_combine_partial(_ptr(y), y.shape[0], _ptr(topk_w), _ptr(dst_row),
-                                     _ptr(rl.pair_rank_row), _ptr(rl.rank_row_token),
-                                     _ptr(rl.rank_offsets), R, rank_rows, T, H, k, _ptr(partial),
-                                     _ptr(status), _stream(y.device))
+    with _on(y.device):
+        code = load().ep_combine_partial(_ptr(y), y.shape[0], _ptr(topk_w), _ptr(dst_row),
+                                         _ptr(rl.pair_rank_row), _ptr(rl.rank_row_token),
+                                         _ptr(rl.rank_offsets), R, rank_rows, T, H, k, _ptr(partial),
+                                         _ptr(status), _stream(y.device))
     _rc("ep_combine_partial", code)
     return partial
 
@@ -318,8 +333,9 @@ def combine_reduce(partial, rl, T, out=None, status=None):
     k = rl.rank_dst_row.shape[1]
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=partial.device)
-    code = load().ep_combine_reduce(_ptr(partial), partial.shape[0], _ptr(rl.rank_dst_row), T, H,
-                                    k, _ptr(out), _ptr(status), _stream(partial.device))
+    with _on(partial.device):
+        code = load().ep_combine_reduce(_ptr(partial), partial.shape[0], _ptr(rl.rank_dst_row), T, H,
+                                        k, _ptr(out), _ptr(status), _stream(partial.device))
     _rc("ep_combine_reduce", code)
     return out
 
@@ -327,7 +343,8 @@ def combine_reduce(partial, rl, T, out=None, status=None):
 def status_read(status):
     """Synchronise the current stream and return the device status word."""
     flags = ctypes.c_uint32(0)
-    code = load().ep_status_read(_ptr(status), _stream(status.device), ctypes.byref(flags))
+    with _on(status.device):
+        code = load().ep_status_read(_ptr(status), _stream(status.device), ctypes.byref(flags))
     _rc("ep_status_read", code)
     return int(flags.value)
 
@@ -379,20 +396,22 @@ class Pipeline:
             if t.is_cuda or not t.is_pinned() or t.dtype != dt or not t.is_contiguous():
                 raise ValueError("%s must be a pinned contiguous host tensor of %s" % (name, dt))
         lay = self.layout
-        code = load().ep_roundtrip_host(
-            self._h, _stream(self.device), _ptr(x_host), _ptr(idx_host), _ptr(w_host), _ptr(out_host),
-            self.T, self.H, self.k, self.E, self.R, LAYOUT_KINDS[self.kind], self.capacity, self.chunk,
-            _ptr(self.x_dev), _ptr(self.idx_dev), _ptr(self.w_dev), _ptr(self.recv),
-            _ptr(self.recv_q), _ptr(self.recv_scale), self.rows,
-            _ptr(self.y), _ptr(self.out_dev), _ptr(lay.expert_counts), _ptr(lay.expert_offsets),
-            _ptr(lay.dst_row), _ptr(lay.rank_token_counts), _ptr(lay.status), _ptr(self.ws),
-            self.ws.numel())
+        with _on(self.device):
+            code = load().ep_roundtrip_host(
+                self._h, _stream(self.device), _ptr(x_host), _ptr(idx_host), _ptr(w_host),
+                _ptr(out_host), self.T, self.H, self.k, self.E, self.R, LAYOUT_KINDS[self.kind],
+                self.capacity, self.chunk, _ptr(self.x_dev), _ptr(self.idx_dev), _ptr(self.w_dev),
+                _ptr(self.recv), _ptr(self.recv_q), _ptr(self.recv_scale), self.rows, _ptr(self.y),
+                _ptr(self.out_dev), _ptr(lay.expert_counts), _ptr(lay.expert_offsets),
+                _ptr(lay.dst_row), _ptr(lay.rank_token_counts), _ptr(lay.status), _ptr(self.ws),
+                self.ws.numel())
         _rc("ep_roundtrip_host", code)
         return out_host
 
     def close(self):
         if getattr(self, "_h", None):
-            load().ep_pipeline_destroy(self._h)
+            with _on(self.device):
+                load().ep_pipeline_destroy(self._h)
             self._h = None
 
     def __del__(self):

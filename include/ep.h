@@ -18,6 +18,8 @@
  *    (allocates and frees) every buffer; the library allocates no device
  *    memory (ep_layout_static_ws uses one fixed array of the library's own;
  *    ep_pipeline_create makes streams and events, no memory).
+ *  - Work runs on the caller's current CUDA device; the pointers and
+ *    `stream` must belong to it.
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Every call only enqueues work on `stream` and returns; nothing
  *    synchronises except ep_status_read().
