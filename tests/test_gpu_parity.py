@@ -440,3 +440,35 @@ def test_combine_large_batch_paths(T, k, H, offset):
     assert np.array_equal(got, oracle.combine_fp32_seq(yb, wb, compact))
     _, r64, absum = oracle.combine_f64(yb, wb, compact)
     check_combine(got, r64, absum, "T=%d k=%d" % (T, k))
+
+
+def test_dispatch_fp8_every_pattern_at_fixed_scales():
+    # blocks of 128 channels: slot 0 holds A (the block amax, which fixes
+    # inv = 448 / max(A, 1e-4)); slots 1..127 hold every finite bf16 pattern of
+    # magnitude <= A, so the conversion of v * inv is checked for all patterns
+    # at each of these scales
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).float().numpy()
+    finite = np.isfinite(vals)
+    rows = []
+    for A in (1e-4, 0.01, 1.0, 3.14159, 448.0, 1e4, 6e4):
+        a_bits = W.bf16_bits(torch.tensor([A], dtype=torch.float32).to(torch.bfloat16))[0]
+        a_val = float(torch.tensor([A]).to(torch.bfloat16).float())
+        sel = pats[finite & (np.abs(vals) <= a_val)]
+        nblk = -(-len(sel) // 127)
+        blk = np.zeros((nblk, 128), np.uint16)
+        blk[:, 0] = a_bits
+        flat = np.zeros(nblk * 127, np.uint16)
+        flat[:len(sel)] = sel
+        blk[:, 1:] = flat.reshape(nblk, 127)
+        rows.append(blk.reshape(-1))
+    allv = np.concatenate(rows)
+    H = 1024
+    allv = np.concatenate([allv, np.zeros((-len(allv)) % H, np.uint16)]).reshape(-1, H)
+    T = allv.shape[0]
+    x = torch.from_numpy(allv.view(np.int16)).view(torch.bfloat16).to(DEV)
+    dst = torch.arange(T, dtype=torch.int32, device=DEV).view(T, 1)
+    q, s = ep.dispatch_fp8(x, dst, T)
+    rq, rs = oracle.dispatch_fp8(allv, dst.cpu().numpy(), T)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
