@@ -351,90 +351,89 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     }
 }
 
-// Small batches (T <= kFusedMaxTokens): the whole layout in one block of NT
-// threads (NT/32 warps of 32 tokens each).  Warp w owns tokens
-// [w*tpw, (w+1)*tpw); per-warp shared histograms give, after an exclusive scan
-// over the warps, each warp's base slot per expert, and the block scan over
-// experts gives the offsets -- the same stable slots as the chunked kernels,
-// in one launch.  One SM does all the work, so larger batches use the
-// chunked kernels, which spread it over the GPU.
+// ---- one-launch layouts for small and medium batches -----------------------
+// Both split their tokens into warp-owned runs.  Each warp builds a shared
+// histogram of its pairs; an exclusive prefix over the warps turns it into
+// the warp's base slot per expert; then the warp walks its pairs 32 at a time
+// in flattened order and ranks equal experts within the piece with
+// popc(peers & lanemask_lt).  Short runs per warp (many warps per block) keep
+// the serial part of the walk short.
+
+// Tokens per launch of the single-block kernel, and its block sizes: blocks
+// of up to 128 tokens and larger ones (up to kFusedMaxTokens).
 constexpr int kFusedMaxTokens = 512;
+#ifndef EP_FUSED_NT_SMALL
+#define EP_FUSED_NT_SMALL 1024
+#endif
+#ifndef EP_FUSED_NT_LARGE
+#define EP_FUSED_NT_LARGE 1024
+#endif
 
+// Per-warp histograms s_w[w * ES + e] (NT/32 warps; row stride ES = E | 1 is
+// odd, so the warps' entries of one expert sit in distinct banks) are
+// replaced by their exclusive prefix over w, and s_sum[e] gets the total.
+// Up to 8 warps: one thread per expert walks the warps.  More: one warp per
+// expert, lane w holding warp w's count, scanned with shuffles.
 template <int NT>
-__global__ void __launch_bounds__(NT)
-layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
-                    int capacity, int align, int tpw, int32_t* __restrict__ expert_counts,
-                    int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
-                    int32_t* __restrict__ rank_token_counts, uint32_t* __restrict__ status) {
-    constexpr int kFusedThreads = NT;
-    constexpr int kFusedWarps = NT / 32;
-    extern __shared__ __align__(16) int32_t smem_i[];
-    const int npad = kFusedWarps * tpw * k;
-    int32_t* s_idx = smem_i;                    // [npad]
-    int32_t* s_w = s_idx + npad;                // [kFusedWarps][E]
-    int32_t* s_tot = s_w + kFusedWarps * E;     // [E]
-    int32_t* s_off = s_tot + E;                 // [E + 1]
-    int32_t* s_rank = s_off + E + 1;            // [R_cols]
-    int32_t* s_rank_of = s_rank + R_cols;       // [E]
-    int32_t* s_warp = s_rank_of + E;            // [kFusedWarps]
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+__device__ __forceinline__ void warp_hist_prefix(int32_t* s_w, int ES, int E, int32_t* s_sum) {
+    constexpr int NW = NT / 32;
+    if constexpr (NW <= 8) {
+        for (int e = threadIdx.x; e < E; e += NT) {
+            int run = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const int v = s_w[w * ES + e];
+                s_w[w * ES + e] = run;
+                run += v;
+            }
+            s_sum[e] = run;
+        }
+    } else {
+        const int lane = threadIdx.x & 31;
+        for (int e = threadIdx.x >> 5; e < E; e += NW) {
+            const int v = lane < NW ? s_w[lane * ES + e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int nb = __shfl_up_sync(kFullMask, incl, o);
+                if (lane >= o) incl += nb;
+            }
+            if (lane < NW) s_w[lane * ES + e] = incl - v;
+            if (lane == 31) s_sum[e] = incl;
+        }
+    }
+}
 
-    pdl_wait();
-    pdl_trigger();
-    if (threadIdx.x == 0 && status) *status = 0u;
-    stage_ids(idx, 0, T * k, npad, s_idx);
-    for (int i = threadIdx.x; i < kFusedWarps * E; i += kFusedThreads) s_w[i] = 0;
-    for (int i = threadIdx.x; i < R_cols; i += kFusedThreads) s_rank[i] = 0;
-    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
-    __syncthreads();
-
-    const int wp0 = warp * tpw * k;
-    const int active_warps = (T + tpw - 1) / tpw;  // warps that own at least one token
-    const bool active = warp < active_warps;       // warp-uniform
-    // pieces holding this warp's pairs (the last active warp may have fewer)
-    const int wpairs = active ? min(tpw * k, T * k - wp0) : 0;
-    const int npieces = (wpairs + 31) / 32;
-    int32_t* my_w = s_w + warp * E;
-    for (int m = 0; m < npieces; ++m) {
-        const int e = s_idx[wp0 + m * 32 + lane];
+// Histogram of one warp's `wpairs` pairs (s_ids) into its row my_w.
+__device__ __forceinline__ void warp_count_pairs(const int32_t* s_ids, int wpairs, int E,
+                                                 int32_t* my_w) {
+    for (int q = threadIdx.x & 31; q < wpairs; q += 32) {
+        const int e = s_ids[q];
         if (e >= 0 && e < E) atomicAdd(&my_w[e], 1);
     }
-    if (R_cols > 0 && active)
-        for (int i = 0; i < tpw; i += 32) {
-            const int t = warp * tpw + i + lane;
-            if (t < T) count_token_ranks(s_idx + t * k, k, E, R_cols, s_rank_of, s_rank);
-        }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kFusedThreads) {
-        int run = 0;
-        for (int w = 0; w < active_warps; ++w) {
-            const int v = s_w[w * E + e];
-            s_w[w * E + e] = run;
-            run += v;
-        }
-        expert_counts[e] = run;
-        s_tot[e] = (run + align - 1) / align * align;  // padded segment length
-    }
-    __syncthreads();
-    block_exclusive_scan<kFusedThreads>(s_tot, E, s_off, s_warp);
-    for (int e = threadIdx.x; e <= E; e += kFusedThreads) expert_offsets[e] = s_off[e];
-    for (int r = threadIdx.x; r < R_cols; r += kFusedThreads) rank_token_counts[r] = s_rank[r];
+}
 
+// Slots of one warp's pairs: slot = s_base[e] (if given) + my_w[e] + the
+// earlier lanes of the piece holding e; my_w[e] then advances by the piece's
+// count of e.  Writes out[0 .. wpairs) and raises the status flags.
+__device__ __forceinline__ void warp_assign_pairs(const int32_t* s_ids, int wpairs, int E, int kind,
+                                                  int capacity, int32_t* my_w,
+                                                  const int32_t* s_base, const int32_t* s_off,
+                                                  int32_t* __restrict__ out, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
     const unsigned lt = lanemask_lt();
     const int key_bits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);
-    const int npairs = T * k;
-    for (int m = 0; m < npieces; ++m) {
-        const int lp = wp0 + m * 32 + lane;
-        const bool in_range = lp < npairs;
-        const int e = s_idx[lp];
+    for (int q0 = 0; q0 < wpairs; q0 += 32) {  // warp-uniform
+        const int q = q0 + lane;
+        const bool in_range = q < wpairs;
+        const int e = in_range ? s_ids[q] : -1;
         const bool valid = (e >= 0) && (e < E);
         const bool bad = in_range && !valid && e != -1;
         const unsigned peers = warp_peers(valid, e, key_bits);
         bool overflow = false;
         int dst = -1;
         if (valid) {
-            const int slot = my_w[e] + __popc(peers & lt);
+            const int slot = (s_base ? s_base[e] : 0) + my_w[e] + __popc(peers & lt);
             if (kind == EP_LAYOUT_CONTIGUOUS) {
                 dst = s_off[e] + slot;
             } else if (slot < capacity) {
@@ -443,7 +442,7 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
                 overflow = true;
             }
         }
-        if (in_range) dst_row[lp] = dst;
+        if (in_range) out[q] = dst;
         __syncwarp();
         if (valid && (__ffs(peers) - 1) == lane) my_w[e] += __popc(peers);
         __syncwarp();
@@ -452,40 +451,102 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     }
 }
 
+// Small batches (T <= kFusedMaxTokens): the whole layout in one block of NT
+// threads; warp w owns tokens [w*tpw, (w+1)*tpw).  The block scan over the
+// expert totals gives the offsets -- the same stable slots as the chunked
+// kernels, in one launch.  One SM does all the work, so larger batches use
+// the cluster or chunked kernels, which spread it over more SMs.
+template <int NT>
+__global__ void __launch_bounds__(NT)
+layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
+                    int capacity, int align, int tpw, int32_t* __restrict__ expert_counts,
+                    int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
+                    int32_t* __restrict__ rank_token_counts, uint32_t* __restrict__ status) {
+    constexpr int NW = NT / 32;
+    extern __shared__ __align__(16) int32_t smem_i[];
+    const int ES = E | 1;
+    const int npairs = T * k;
+    const int npad = NW * tpw * k;              // >= npairs
+    int32_t* s_idx = smem_i;                    // [npad]
+    int32_t* s_w = s_idx + npad;                // [NW][ES]
+    int32_t* s_tot = s_w + NW * ES;             // [E]
+    int32_t* s_off = s_tot + E;                 // [E + 1]
+    int32_t* s_rank = s_off + E + 1;            // [R_cols]
+    int32_t* s_rank_of = s_rank + R_cols;       // [E]
+    int32_t* s_warp = s_rank_of + E;            // [NW]
+    const int warp = threadIdx.x >> 5;
+
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0 && status) *status = 0u;
+    stage_ids(idx, 0, npairs, npad, s_idx);
+    for (int i = threadIdx.x; i < NW * ES; i += NT) s_w[i] = 0;
+    for (int i = threadIdx.x; i < R_cols; i += NT) s_rank[i] = 0;
+    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
+    __syncthreads();
+
+    const int wp0 = warp * tpw * k;
+    const int wrem = npairs - wp0;
+    const int wpairs = wrem <= 0 ? 0 : (wrem < tpw * k ? wrem : tpw * k);
+    int32_t* my_w = s_w + warp * ES;
+    warp_count_pairs(s_idx + wp0, wpairs, E, my_w);
+    if (R_cols > 0)
+        for (int t = threadIdx.x; t < T; t += NT)
+            count_token_ranks(s_idx + t * k, k, E, R_cols, s_rank_of, s_rank);
+    __syncthreads();
+    warp_hist_prefix<NT>(s_w, ES, E, s_tot);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += NT) {
+        const int c = s_tot[e];
+        expert_counts[e] = c;
+        s_tot[e] = (c + align - 1) / align * align;  // padded segment length
+    }
+    __syncthreads();
+    block_exclusive_scan<NT>(s_tot, E, s_off, s_warp);
+    for (int e = threadIdx.x; e <= E; e += NT) expert_offsets[e] = s_off[e];
+    for (int r = threadIdx.x; r < R_cols; r += NT) rank_token_counts[r] = s_rank[r];
+
+    warp_assign_pairs(s_idx + wp0, wpairs, E, kind, capacity, my_w, nullptr, s_off, dst_row + wp0,
+                      status);
+}
+
 // Medium batches (T <= kClusterMaxTokens): the whole layout in ONE launch of
-// one 8-block thread-block cluster.  Each block owns 256 tokens (a warp per
-// 32) and builds its per-warp expert histograms; after a cluster barrier
-// every block reads the 8 block histograms through distributed shared memory
-// (the blocks before it give its base slots, all of them the totals), and a
-// second cluster barrier keeps every block resident until all remote reads
-// are done.  The barriers are hardware cluster barriers: no block ever spins
-// on memory.
+// one 8-block thread-block cluster.  Each block owns 256 tokens and builds
+// per-warp expert histograms; after a cluster barrier every block reads the 8
+// block totals through distributed shared memory (the blocks before it give
+// its base slots, all of them the totals), and a second cluster barrier keeps
+// every block resident until all remote reads are done.  The barriers are
+// hardware cluster barriers: no block ever spins on memory.
 namespace cg = cooperative_groups;
 constexpr int kClusterBlocks = 8;
-constexpr int kClusterThreads = 256;
-constexpr int kClusterWarps = kClusterThreads / 32;
-constexpr int kClusterTokens = kClusterThreads;  // tokens per block
+constexpr int kClusterTokens = 256;  // tokens per block
 constexpr int kClusterMaxTokens = kClusterBlocks * kClusterTokens;
+#ifndef EP_CLUSTER_NT
+#define EP_CLUSTER_NT 1024
+#endif
 
-__global__ void __launch_bounds__(kClusterThreads)
+template <int NT>
+__global__ void __launch_bounds__(NT)
 layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
                       int capacity, int align, int32_t* __restrict__ expert_counts,
                       int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
                       int32_t* __restrict__ rank_token_counts, uint32_t* __restrict__ status) {
+    constexpr int NW = NT / 32;
+    constexpr int TPW = kClusterTokens / NW;      // tokens per warp
     cg::cluster_group cluster = cg::this_cluster();
     const int b = (int)cluster.block_rank();
     extern __shared__ __align__(16) int32_t smem_i[];
+    const int ES = E | 1;
     const int npad = kClusterTokens * k;
     int32_t* s_idx = smem_i;                      // [npad]
-    int32_t* s_w = s_idx + npad;                  // [kClusterWarps][E]
-    int32_t* s_hist = s_w + kClusterWarps * E;    // [E + R_cols]  block totals (read remotely)
+    int32_t* s_w = s_idx + npad;                  // [NW][ES]
+    int32_t* s_hist = s_w + NW * ES;              // [E + R_cols]  block totals (read remotely)
     int32_t* s_tot = s_hist + E + R_cols;         // [E]
     int32_t* s_base = s_tot + E;                  // [E]
     int32_t* s_off = s_base + E;                  // [E + 1]
     int32_t* s_rank_of = s_off + E + 1;           // [E]
     int32_t* s_rank = s_rank_of + E;              // [R_cols]
-    int32_t* s_warp = s_rank + R_cols;            // [kClusterWarps]
-    const int lane = threadIdx.x & 31;
+    int32_t* s_warp = s_rank + R_cols;            // [NW]
     const int warp = threadIdx.x >> 5;
     const int t0 = b * kClusterTokens;
     const int ntok = T - t0 < 0 ? 0 : (T - t0 < kClusterTokens ? T - t0 : kClusterTokens);
@@ -494,36 +555,25 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
     pdl_trigger();
     if (b == 0 && threadIdx.x == 0 && status) *status = 0u;
     stage_ids(idx, (int64_t)t0 * k, ntok * k, npad, s_idx);
-    for (int i = threadIdx.x; i < kClusterWarps * E; i += kClusterThreads) s_w[i] = 0;
-    for (int i = threadIdx.x; i < R_cols; i += kClusterThreads) s_rank[i] = 0;
+    for (int i = threadIdx.x; i < NW * ES; i += NT) s_w[i] = 0;
+    for (int i = threadIdx.x; i < R_cols; i += NT) s_rank[i] = 0;
     if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
     __syncthreads();
 
-    const int wp0 = warp * 32 * k;
-    const int wtok = ntok - warp * 32;                           // tokens of this warp
-    const int npieces = wtok <= 0 ? 0 : ((wtok < 32 ? wtok : 32) * k + 31) / 32;
-    int32_t* my_w = s_w + warp * E;
-    for (int m = 0; m < npieces; ++m) {
-        const int e = s_idx[wp0 + m * 32 + lane];
-        if (e >= 0 && e < E) atomicAdd(&my_w[e], 1);
-    }
-    if (R_cols > 0 && threadIdx.x < ntok)
-        count_token_ranks(s_idx + threadIdx.x * k, k, E, R_cols, s_rank_of, s_rank);
+    const int wp0 = warp * TPW * k;
+    const int wrem = ntok * k - wp0;
+    const int wpairs = wrem <= 0 ? 0 : (wrem < TPW * k ? wrem : TPW * k);
+    int32_t* my_w = s_w + warp * ES;
+    warp_count_pairs(s_idx + wp0, wpairs, E, my_w);
+    if (R_cols > 0)
+        for (int t = threadIdx.x; t < ntok; t += NT)
+            count_token_ranks(s_idx + t * k, k, E, R_cols, s_rank_of, s_rank);
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kClusterThreads) {
-        int run = 0;
-#pragma unroll
-        for (int w = 0; w < kClusterWarps; ++w) {
-            const int v = s_w[w * E + e];
-            s_w[w * E + e] = run;
-            run += v;
-        }
-        s_hist[e] = run;
-    }
-    for (int r = threadIdx.x; r < R_cols; r += kClusterThreads) s_hist[E + r] = s_rank[r];
+    warp_hist_prefix<NT>(s_w, ES, E, s_hist);
+    for (int r = threadIdx.x; r < R_cols; r += NT) s_hist[E + r] = s_rank[r];
     cluster.sync();  // every block's histogram is complete and visible
 
-    for (int e = threadIdx.x; e < E; e += kClusterThreads) {
+    for (int e = threadIdx.x; e < E; e += NT) {
         int before = 0, total = 0;
 #pragma unroll
         for (int q = 0; q < kClusterBlocks; ++q) {
@@ -536,7 +586,7 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
         if (b == 0) expert_counts[e] = total;
     }
     if (b == 0 && rank_token_counts)
-        for (int r = threadIdx.x; r < R_cols; r += kClusterThreads) {
+        for (int r = threadIdx.x; r < R_cols; r += NT) {
             int total = 0;
 #pragma unroll
             for (int q = 0; q < kClusterBlocks; ++q) total += cluster.map_shared_rank(s_hist, q)[E + r];
@@ -544,40 +594,12 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
         }
     cluster.sync();  // no block leaves while another still reads its histogram
 
-    block_exclusive_scan<kClusterThreads>(s_tot, E, s_off, s_warp);
+    block_exclusive_scan<NT>(s_tot, E, s_off, s_warp);
     if (b == 0)
-        for (int e = threadIdx.x; e <= E; e += kClusterThreads) expert_offsets[e] = s_off[e];
+        for (int e = threadIdx.x; e <= E; e += NT) expert_offsets[e] = s_off[e];
 
-    const unsigned lt = lanemask_lt();
-    const int key_bits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);
-    const int npairs = ntok * k;
-    int32_t* out = dst_row + (int64_t)t0 * k;
-    for (int m = 0; m < npieces; ++m) {
-        const int lp = wp0 + m * 32 + lane;
-        const bool in_range = lp < npairs;
-        const int e = s_idx[lp];
-        const bool valid = (e >= 0) && (e < E);
-        const bool bad = in_range && !valid && e != -1;
-        const unsigned peers = warp_peers(valid, e, key_bits);
-        bool overflow = false;
-        int dst = -1;
-        if (valid) {
-            const int slot = s_base[e] + my_w[e] + __popc(peers & lt);
-            if (kind == EP_LAYOUT_CONTIGUOUS) {
-                dst = s_off[e] + slot;
-            } else if (slot < capacity) {
-                dst = e * capacity + slot;
-            } else {
-                overflow = true;
-            }
-        }
-        if (in_range) out[lp] = dst;
-        __syncwarp();
-        if (valid && (__ffs(peers) - 1) == lane) my_w[e] += __popc(peers);
-        __syncwarp();
-        warp_flag(status, bad, EP_FLAG_BAD_EXPERT);
-        warp_flag(status, overflow, EP_FLAG_OVERFLOW);
-    }
+    warp_assign_pairs(s_idx + wp0, wpairs, E, kind, capacity, my_w, s_base, s_off,
+                      dst_row + (int64_t)t0 * k + wp0, status);
 }
 
 // T == 0: write the (all-zero) outputs so that callers always get defined data.
@@ -605,61 +627,87 @@ size_t assign_smem_bytes(int k, int E) {
 }
 
 size_t fused_smem_bytes(int warps, int tpw, int k, int E, int R_cols) {
-    return ((size_t)warps * tpw * k + (size_t)warps * E + 3 * (size_t)E + 1 + R_cols + warps) *
-           sizeof(int32_t);
+    return ((size_t)warps * tpw * k + (size_t)warps * (E | 1) + 3 * (size_t)E + 1 + R_cols +
+            warps) * sizeof(int32_t);
 }
 
 constexpr size_t kFusedSmemLimit = 160 * 1024;
 
-template <int NT>
-cudaError_t launch_fused(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols, int kind,
-                         int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
-                         int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
-                         size_t smem, cudaStream_t stream) {
-    // raise the kernel's shared-memory limit once per device (to the largest
-    // size this path ever requests)
-    static std::atomic<uint64_t> configured{0};
+// Raise a kernel's dynamic shared-memory limit to kFusedSmemLimit, once per
+// device and kernel (the flag word is the caller's, one per kernel).
+template <typename K>
+cudaError_t raise_smem_limit(K kernel, std::atomic<uint64_t>& configured) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        err = cudaFuncSetAttribute(layout_fused_kernel<NT>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)kFusedSmemLimit);
         if (err != cudaSuccess) return err;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
+    return cudaSuccess;
+}
+
+template <int NT>
+cudaError_t launch_fused(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols, int kind,
+                         int capacity, int align, int tpw, int32_t* expert_counts,
+                         int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
+                         uint32_t* status, size_t smem, cudaStream_t stream) {
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t err = raise_smem_limit(layout_fused_kernel<NT>, configured);
+    if (err != cudaSuccess) return err;
     return launch_pdl(layout_fused_kernel<NT>, dim3(1), dim3(NT), smem, stream, topk_idx, (int)T,
-                      k, E, R_cols, kind, capacity, align, 32, expert_counts, expert_offsets,
+                      k, E, R_cols, kind, capacity, align, tpw, expert_counts, expert_offsets,
                       dst_row, rank_token_counts, status);
 }
 
-size_t cluster_smem_bytes(int k, int E, int R_cols) {
-    return ((size_t)kClusterTokens * k + (size_t)kClusterWarps * E + (E + R_cols) + 3 * (size_t)E +
-            1 + E + R_cols + kClusterWarps) *
-           sizeof(int32_t);
+// The single-block layout with the largest block (down to 128 threads, from
+// `nt`) whose shared memory fits; cudaErrorNotSupported if none does.
+cudaError_t try_fused(int nt, const int32_t* topk_idx, int64_t T, int k, int E, int R_cols,
+                      int kind, int capacity, int align, int32_t* expert_counts,
+                      int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
+                      uint32_t* status, cudaStream_t stream) {
+    for (; nt >= 128; nt /= 2) {
+        if (nt != 1024 && nt != 512 && nt != 256 && nt != 128) continue;
+        const int warps = nt / 32;
+        const int tpw = (int)((T + warps - 1) / warps);
+        const size_t smem = fused_smem_bytes(warps, tpw, k, E, R_cols);
+        if (smem > kFusedSmemLimit) continue;
+#define EP_FUSED_CASE(N)                                                                       \
+    case N:                                                                                    \
+        return launch_fused<N>(topk_idx, T, k, E, R_cols, kind, capacity, align, tpw,          \
+                               expert_counts, expert_offsets, dst_row, rank_token_counts,      \
+                               status, smem, stream);
+        switch (nt) {
+            EP_FUSED_CASE(1024)
+            EP_FUSED_CASE(512)
+            EP_FUSED_CASE(256)
+            EP_FUSED_CASE(128)
+        }
+#undef EP_FUSED_CASE
+    }
+    return cudaErrorNotSupported;
 }
 
+size_t cluster_smem_bytes(int nt, int k, int E, int R_cols) {
+    const size_t warps = nt / 32;
+    return ((size_t)kClusterTokens * k + warps * (E | 1) + 5 * (size_t)E + 1 + 2 * (size_t)R_cols +
+            warps) * sizeof(int32_t);
+}
+
+template <int NT>
 cudaError_t launch_cluster(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols, int kind,
                            int capacity, int align, int32_t* expert_counts,
                            int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
                            uint32_t* status, size_t smem, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    cudaError_t err = raise_smem_limit(layout_cluster_kernel<NT>, configured);
     if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-        err = cudaFuncSetAttribute(layout_cluster_kernel,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kFusedSmemLimit);
-        if (err != cudaSuccess) return err;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kClusterBlocks);
-    cfg.blockDim = dim3(kClusterThreads);
+    cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -671,9 +719,34 @@ cudaError_t launch_cluster(const int32_t* topk_idx, int64_t T, int k, int E, int
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, topk_idx, (int)T, k, E, R_cols, kind,
-                              capacity, align, expert_counts, expert_offsets, dst_row,
+    return cudaLaunchKernelEx(&cfg, layout_cluster_kernel<NT>, topk_idx, (int)T, k, E, R_cols,
+                              kind, capacity, align, expert_counts, expert_offsets, dst_row,
                               rank_token_counts, status);
+}
+
+// The cluster layout with the largest block (down to 256 threads, from `nt`)
+// whose shared memory fits; cudaErrorNotSupported if none does.
+cudaError_t try_cluster(int nt, const int32_t* topk_idx, int64_t T, int k, int E, int R_cols,
+                        int kind, int capacity, int align, int32_t* expert_counts,
+                        int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
+                        uint32_t* status, cudaStream_t stream) {
+    for (; nt >= 256; nt /= 2) {
+        if (nt != 1024 && nt != 512 && nt != 256) continue;
+        const size_t smem = cluster_smem_bytes(nt, k, E, R_cols);
+        if (smem > kFusedSmemLimit) continue;
+#define EP_CLUSTER_CASE(N)                                                                     \
+    case N:                                                                                    \
+        return launch_cluster<N>(topk_idx, T, k, E, R_cols, kind, capacity, align,             \
+                                 expert_counts, expert_offsets, dst_row, rank_token_counts,    \
+                                 status, smem, stream);
+        switch (nt) {
+            EP_CLUSTER_CASE(1024)
+            EP_CLUSTER_CASE(512)
+            EP_CLUSTER_CASE(256)
+        }
+#undef EP_CLUSTER_CASE
+    }
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
@@ -687,25 +760,17 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                           expert_offsets, rank_token_counts, status);
     const int R_cols = rank_token_counts ? R : 0;
     if (T <= kFusedMaxTokens) {
-        // one warp per 32 tokens: 128 threads up to 128 tokens, else 512
-        const int nt = T <= 128 ? 128 : 512;
-        const size_t smem = fused_smem_bytes(nt / 32, 32, k, E, R_cols);
-        if (smem <= kFusedSmemLimit) {
-            if (nt == 128)
-                return launch_fused<128>(topk_idx, T, k, E, R_cols, kind, capacity, align,
-                                         expert_counts, expert_offsets, dst_row,
-                                         rank_token_counts, status, smem, stream);
-            return launch_fused<512>(topk_idx, T, k, E, R_cols, kind, capacity, align,
-                                     expert_counts, expert_offsets, dst_row, rank_token_counts,
-                                     status, smem, stream);
-        }
+        const cudaError_t err =
+            try_fused(T <= 128 ? EP_FUSED_NT_SMALL : EP_FUSED_NT_LARGE, topk_idx, T, k, E, R_cols,
+                      kind, capacity, align, expert_counts, expert_offsets, dst_row,
+                      rank_token_counts, status, stream);
+        if (err != cudaErrorNotSupported) return err;
     }
     if (T <= kClusterMaxTokens) {
-        const size_t smem = cluster_smem_bytes(k, E, R_cols);
-        if (smem <= kFusedSmemLimit)
-            return launch_cluster(topk_idx, T, k, E, R_cols, kind, capacity, align, expert_counts,
-                                  expert_offsets, dst_row, rank_token_counts, status, smem,
-                                  stream);
+        const cudaError_t err =
+            try_cluster(EP_CLUSTER_NT, topk_idx, T, k, E, R_cols, kind, capacity, align,
+                        expert_counts, expert_offsets, dst_row, rank_token_counts, status, stream);
+        if (err != cudaErrorNotSupported) return err;
     }
     const int64_t nchunk = layout_num_chunks(T);
     const int ncol = E + R_cols;
