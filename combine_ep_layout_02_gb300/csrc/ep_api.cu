@@ -2,6 +2,8 @@
 // Every check that can fail happens before anything is enqueued.
 #include <stdint.h>
 
+#include <atomic>
+
 #include "ep_internal.cuh"
 
 namespace {
@@ -31,6 +33,26 @@ int check_rows_args(int64_t T, int64_t H, int k, int64_t rows) {
 
 namespace ep {
 void record_cuda_error(int err) { g_last_cuda_error = err; }
+
+RowSlices row_slices(int64_t T, int64_t nvec) {
+    // SM count per device, read once (it only shapes grids)
+    static std::atomic<int> sm_cache[64];
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        sms = sm_cache[dev & 63].load(std::memory_order_relaxed);
+        if (sms == 0 &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            sms > 0)
+            sm_cache[dev & 63].store(sms, std::memory_order_relaxed);
+    }
+    if (sms <= 0) sms = 1;
+    const int64_t target = (int64_t)sms * EP_SLICE_WARPS_PER_SM;
+    int64_t S = 1;
+    while (T * S < target && (nvec + 2 * S - 1) / (2 * S) >= 32) S *= 2;
+    if (S == 1) return RowSlices{1, nvec};
+    const int64_t slice = ((nvec + S - 1) / S + 31) / 32 * 32;
+    return RowSlices{(int)((nvec + slice - 1) / slice), slice};
+}
 }  // namespace ep
 
 extern "C" {

@@ -1,8 +1,9 @@
 // ep_combine.cu -- weighted top-k combine: out[t] = bf16(sum_j w[t,j] *
 // y[dst_row[t,j]]), accumulated in fp32 fused multiply-adds in increasing j.
 //
-// One warp per token.  Per iteration each lane owns 8 channels (one 16-byte
-// vector) of U column groups; the loads of all k rows for those groups are
+// One warp per token (per column slice of the token when there are few
+// tokens).  Per iteration each lane owns 8 channels (one 16-byte vector) of U
+// column groups; the loads of all k rows for those groups are
 // issued before any arithmetic so that k*U 16-byte loads per lane are in
 // flight, then the FMAs run in j order (the order fixes the fp32 result
 // bit-for-bit).  Every expert-output byte is read once and every output byte
@@ -30,11 +31,12 @@ constexpr int kCombineWarps = EP_COMBINE_WARPS;
 constexpr int kRowBatch = 8;  // rows whose loads are issued together
 
 // Accumulate one batch of up to kRowBatch rows into acc for the U column
-// groups starting at v0: all loads first, then the FMAs in j order.
+// groups starting at v0 (vectors below vend only): all loads first, then the
+// FMAs in j order.
 template <int U>
 __device__ __forceinline__ void accumulate_batch(const uint4* const (&src)[kRowBatch],
                                                  const float (&wj)[kRowBatch], int64_t v0,
-                                                 int64_t nvec, int lane, float (&acc)[U][8]) {
+                                                 int64_t vend, int lane, float (&acc)[U][8]) {
     uint4 buf[kRowBatch][U];
 #pragma unroll
     for (int jj = 0; jj < kRowBatch; ++jj) {
@@ -42,7 +44,7 @@ __device__ __forceinline__ void accumulate_batch(const uint4* const (&src)[kRowB
         for (int u = 0; u < U; ++u) {
             const int64_t v = v0 + u * 32 + lane;
             buf[jj][u] = make_uint4(0, 0, 0, 0);
-            if (src[jj] != nullptr && v < nvec) buf[jj][u] = ld_stream_v4(src[jj] + v);
+            if (src[jj] != nullptr && v < vend) buf[jj][u] = ld_stream_v4(src[jj] + v);
         }
     }
 #pragma unroll
@@ -62,12 +64,12 @@ __device__ __forceinline__ void accumulate_batch(const uint4* const (&src)[kRowB
 }
 
 template <int U>
-__device__ __forceinline__ void store_bf16(uint4* out_row, int64_t v0, int64_t nvec, int lane,
+__device__ __forceinline__ void store_bf16(uint4* out_row, int64_t v0, int64_t vend, int lane,
                                            const float (&acc)[U][8]) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t v = v0 + u * 32 + lane;
-        if (v < nvec) {
+        if (v < vend) {
             uint4 o;
             o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
             o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
@@ -81,13 +83,17 @@ __device__ __forceinline__ void store_bf16(uint4* out_row, int64_t v0, int64_t n
 template <int U>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
-               const int32_t* __restrict__ dst_row, int64_t T, int64_t nvec, int k, int64_t rows,
-               uint4* __restrict__ out, uint32_t* __restrict__ status) {
+               const int32_t* __restrict__ dst_row, int64_t T, int64_t nvec, int k, int S,
+               int64_t slice, int64_t rows, uint4* __restrict__ out,
+               uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    const int64_t g = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    const int64_t t = g / S;
     if (t >= T) return;  // warp-uniform
+    const int64_t vb = (g - t * S) * slice;          // this warp's column slice [vb, ve)
+    const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
 
     int my_row = -1;
     float my_w = 0.0f;
@@ -113,19 +119,19 @@ combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
             wj[jj] = __shfl_sync(kFullMask, my_w, jj);
             src[jj] = (jj < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
         }
-        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+        for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
             float acc[U][8];
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-            accumulate_batch<U>(src, wj, v0, nvec, lane, acc);
-            store_bf16<U>(out_row, v0, nvec, lane, acc);
+            accumulate_batch<U>(src, wj, v0, ve, lane, acc);
+            store_bf16<U>(out_row, v0, ve, lane, acc);
         }
         return;
     }
     // k > kRowBatch: batches of kRowBatch rows inside each column group
-    for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+    for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
         float acc[U][8];
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -141,9 +147,9 @@ combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
                 wj[jj] = __shfl_sync(kFullMask, my_w, j & 31);
                 src[jj] = (j < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
             }
-            accumulate_batch<U>(src, wj, v0, nvec, lane, acc);
+            accumulate_batch<U>(src, wj, v0, ve, lane, acc);
         }
-        store_bf16<U>(out_row, v0, nvec, lane, acc);
+        store_bf16<U>(out_row, v0, ve, lane, acc);
     }
 }
 
@@ -265,10 +271,11 @@ cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* ds
                           static_cast<Vec32*>(out), status);
     }
     const int64_t nvec = H / 8;
-    const unsigned grid = (unsigned)((T + kCombineWarps - 1) / kCombineWarps);
+    const RowSlices sl = row_slices(T, nvec);
+    const unsigned grid = (unsigned)((T * sl.S + kCombineWarps - 1) / kCombineWarps);
     return launch_pdl(combine_kernel<EP_COMBINE_U>, dim3(grid), dim3(kCombineWarps * 32), 0, stream,
-                      static_cast<const uint4*>(y), topk_w, dst_row, T, nvec, k, rows,
-                      static_cast<uint4*>(out), status);
+                      static_cast<const uint4*>(y), topk_w, dst_row, T, nvec, k, sl.S, sl.slice,
+                      rows, static_cast<uint4*>(out), status);
 }
 
 }  // namespace ep

@@ -1,8 +1,9 @@
 // ep_dispatch.cu -- BF16 dispatch: scatter of token rows into the
 // per-expert buffer (bit copy).  The FP8 variant is in ep_dispatch_fp8.cu.
 //
-// One warp per token.  The warp reads the token row once in 16-byte vectors
-// (streaming, no L1 allocation) and writes it to each of its k destination
+// One warp per token (per column slice of the token when there are few
+// tokens).  The warp reads its part of the row once in 16-byte vectors
+// (streaming, no L1 allocation) and writes it to each of the k destination
 // rows, so every input byte is read once and every output byte written once:
 // the HBM floor is T*H*2 read + T*k*H*2 written.
 #include "ep_internal.cuh"
@@ -28,17 +29,20 @@ constexpr int kRowRegs = 8;        // destination rows held in registers per pas
 
 template <int U>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
-dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k,
-                     const int32_t* __restrict__ dst_row, uint4* __restrict__ recv, int64_t rows,
-                     uint32_t* __restrict__ status) {
+dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k, int S,
+                     int64_t slice, const int32_t* __restrict__ dst_row, uint4* __restrict__ recv,
+                     int64_t rows, uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
+    const int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
+    const int64_t t = g / S;
     if (t >= T) return;  // warp-uniform
+    const int64_t vb = (g - t * S) * slice;          // this warp's column slice [vb, ve)
+    const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
     const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const uint4* src = x + t * nvec;
-    // k <= 8 is one pass; larger k re-reads the row once per 8 destinations
+    // k <= 8 is one pass; larger k re-reads the slice once per 8 destinations
     for (int j0 = 0; j0 < k; j0 += kRowRegs) {
         uint4* dst[kRowRegs];
 #pragma unroll
@@ -46,12 +50,12 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
             const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
             dst[jj] = (j0 + jj < k && r >= 0) ? recv + (int64_t)r * nvec : nullptr;
         }
-        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+        for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
             uint4 buf[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + u * 32 + lane;
-                if (v < nvec) buf[u] = ld_stream_v4(src + v);
+                if (v < ve) buf[u] = ld_stream_v4(src + v);
             }
 #pragma unroll
             for (int jj = 0; jj < kRowRegs; ++jj) {
@@ -59,7 +63,7 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t v = v0 + u * 32 + lane;
-                    if (v < nvec) {
+                    if (v < ve) {
                         if (EP_DISPATCH_STORE_CS) st_cs_v4(dst[jj] + v, buf[u]);
                         else st_v4(dst[jj] + v, buf[u]);
                     }
@@ -166,10 +170,11 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
     }
 #endif
     const int64_t nvec = H / 8;
-    const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
-    return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U>, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
-                      static_cast<const uint4*>(x), T, nvec, k, dst_row, static_cast<uint4*>(recv),
-                      rows, status);
+    const RowSlices sl = row_slices(T, nvec);
+    const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
+    return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U>, dim3(grid), dim3(kDispatchWarps * 32), 0,
+                      stream, static_cast<const uint4*>(x), T, nvec, k, sl.S, sl.slice, dst_row,
+                      static_cast<uint4*>(recv), rows, status);
 }
 
 }  // namespace ep

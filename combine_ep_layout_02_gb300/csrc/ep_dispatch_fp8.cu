@@ -1,5 +1,6 @@
 // ep_dispatch_fp8.cu -- dispatch with the per-token FP8 e4m3 cast fused into
-// the copy.  One warp per token: each lane owns 16 consecutive channels, 8
+// the copy.  One warp per token (per 512-channel-aligned slice of the token
+// when there are few tokens): each lane owns 16 consecutive channels, 8
 // lanes form one 128-channel block whose amax comes from three xor-shuffles,
 // so the cast costs no extra pass over memory (PR #1238 measures the unfused
 // cast as a separate launch-bound step).  Every input byte is read once and
@@ -69,15 +70,21 @@ __device__ __forceinline__ Fp8Group quantize16(const uint4& a, const uint4& b) {
 
 static_assert(kDispatchWarps * 32 == 256, "EP_FP8_BOUNDS assumes 256-thread blocks");
 __global__ void EP_FP8_BOUNDS
-dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
-                    const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv_q,
-                    float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status) {
+dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k, int S,
+                    int64_t slice_ch, const int32_t* __restrict__ dst_row,
+                    uint8_t* __restrict__ recv_q, float* __restrict__ recv_scale, int64_t rows,
+                    uint32_t* __restrict__ status) {
     constexpr int U = EP_FP8_U;
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
+    const int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
+    const int64_t t = g / S;
     if (t >= T) return;
+    // this warp's channels [cb, ce): multiples of 512 (S > 1) or the whole row,
+    // so that all 8 lanes of a 128-channel block agree on every bound below
+    const int64_t cb = (g - t * S) * slice_ch;
+    const int64_t ce = cb + slice_ch < H ? cb + slice_ch : H;
     const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const int64_t nblk = H / 128;
     const uint16_t* src = x + t * H;
@@ -88,14 +95,14 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
             const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
             rr[jj] = (j0 + jj < k) ? r : -1;
         }
-        for (int64_t c0 = 0; c0 < H; c0 += 512 * U) {
+        for (int64_t c0 = cb; c0 < ce; c0 += 512 * U) {
             uint4 a[U], b[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t c = c0 + u * 512 + lane * 16;
                 a[u] = make_uint4(0, 0, 0, 0);
                 b[u] = make_uint4(0, 0, 0, 0);
-                if (c < H) {  // H % 128 == 0: all 8 lanes of a block agree
+                if (c < ce) {  // H % 128 == 0: all 8 lanes of a block agree
 #if EP_FP8_LOAD32
                     const Vec32 v = ld_stream_v8(src + c);  // 32-byte aligned: H % 128 == 0
                     a[u] = v.lo;
@@ -109,7 +116,7 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t c = c0 + u * 512 + lane * 16;
-                const bool act = c < H;
+                const bool act = c < ce;
                 const Fp8Group g = quantize16(a[u], b[u]);
                 const bool scale_writer = act && (lane & 7) == 0;
 #pragma unroll
@@ -130,10 +137,12 @@ cudaError_t launch_dispatch_fp8(const void* x, int64_t T, int64_t H, int k,
                                 const int32_t* dst_row, uint8_t* recv_q, float* recv_scale,
                                 int64_t rows, uint32_t* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((T + kDispatchWarps - 1) / kDispatchWarps);
+    // slices in units of one lane's 16 channels (32 units = one 512-channel group)
+    const RowSlices sl = row_slices(T, H / 16);
+    const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
     return launch_pdl(dispatch_fp8_kernel, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
-                      static_cast<const uint16_t*>(x), T, H, k, dst_row, recv_q, recv_scale, rows,
-                      status);
+                      static_cast<const uint16_t*>(x), T, H, k, sl.S, sl.slice * 16, dst_row,
+                      recv_q, recv_scale, rows, status);
 }
 
 }  // namespace ep

@@ -228,6 +228,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Column slices of the token-row kernels (BF16 dispatch, combine).  One warp
+// per token leaves most SMs idle when there are few tokens, so each row is
+// then split into S slices of `slice` 16-byte vectors (a multiple of 32: one
+// vector per lane), one warp per (token, slice).  S doubles while the grid is
+// below EP_SLICE_WARPS_PER_SM warps per SM and the slices stay >= 32 vectors;
+// S = 1 (slice = nvec) otherwise.  The choice only shapes the grid: every
+// output element is still computed by exactly one lane, in the same order.
+#ifndef EP_SLICE_WARPS_PER_SM
+#define EP_SLICE_WARPS_PER_SM 8
+#endif
+struct RowSlices {
+    int S;          // slices (warps) per token
+    int64_t slice;  // 16-byte vectors per slice
+};
+RowSlices row_slices(int64_t T, int64_t nvec);
+
 // Tokens per layout chunk (one per thread of a 128-thread block).
 constexpr int kLayoutThreads = 128;
 constexpr int kLayoutWarps = kLayoutThreads / 32;

@@ -119,6 +119,33 @@ def test_dispatch_bf16_bit_exact(name, T, H):
     assert ep.status_read(lay.status) == 0
 
 
+@pytest.mark.parametrize("T,k,H,E", [(1, 8, 2048, 64), (3, 13, 1336, 32), (37, 8, 7168, 256),
+                                     (5, 1, 1664, 8), (200, 8, 384, 16), (64, 32, 4096, 1024)])
+def test_few_tokens_column_slices(T, k, H, E):
+    # with few tokens the row kernels (BF16 and FP8 dispatch, combine) split
+    # each row into column slices, one warp each; these shapes give single,
+    # ragged and unsplit rows, k above the 8 rows held in registers, and
+    # FP8 slices of 512-channel groups with a short last slice
+    g = torch.Generator().manual_seed(T * 1000 + H)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    x = (torch.randn(T, H, generator=g) * 3).to(torch.bfloat16)
+    w = torch.rand(T, k, generator=g) - 0.25
+    y = torch.randn(T * k, H, generator=g).to(torch.bfloat16)
+    lay = ep.layout(idx.to(DEV), E, 1)
+    rows = T * k
+    dst = lay.dst_row.cpu().numpy()
+    recv = ep.dispatch(x.to(DEV), lay.dst_row, rows, status=lay.status)
+    assert np.array_equal(_bits(recv), oracle.dispatch_bf16(_bits(x), dst, rows))
+    out = ep.combine(y.to(DEV), w.to(DEV), lay.dst_row, status=lay.status)
+    assert np.array_equal(_bits(out), oracle.combine_fp32_seq(_bits(y), w.numpy(), dst))
+    if H % 128 == 0:
+        q, s = ep.dispatch_fp8(x.to(DEV), lay.dst_row, rows, status=lay.status)
+        rq, rs = oracle.dispatch_fp8(_bits(x), dst, rows)
+        assert np.array_equal(q.cpu().numpy(), rq)
+        assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert ep.status_read(lay.status) == 0
+
+
 def test_dispatch_bad_rows_are_skipped_and_flagged():
     x = torch.randn(4, 64, device=DEV).to(torch.bfloat16)
     dst = torch.tensor([[0, 9], [1, -1], [-3, 2], [3, 4]], dtype=torch.int32, device=DEV)
