@@ -548,9 +548,21 @@ def run_ours(args, rank, world, local):
     }
     per_launch_ms = {"layout": lay_ms / args.steps, "dispatch": disp_ms / args.steps,
                      "combine": comb_ms / args.steps}
+    if args.path == "two_stage":
+        # each timed stage is two kernels; nr = rank rows the route fills
+        nr = int(rl.rank_offsets[-1])
+        alg = {
+            "layout": 2 * Tk * 4 + Tk * 4 + 2 * Tk * 4 + nr * 4,
+            "dispatch": (wl.T * wl.H * 2 + nr * wl.H * 2 + Tk * 4)          # copy to ranks
+                        + (nr * wl.H * 2 + Tk * wl.H * 2 + 2 * Tk * 4),     # expansion
+            "combine": (Tk * wl.H * 2 + nr * wl.H * 2 + Tk * 12 + nr * 4)   # rank-local partials
+                       + (nr * wl.H * 2 + wl.T * wl.H * 2 + Tk * 4),       # final reduce
+        }
     dominant = max(("dispatch", "combine"), key=lambda n: per_launch_ms[n])
     peak, peak_src = measured_peak()
     kname = "dispatch_fp8" if (dominant == "dispatch" and wl.payload == "fp8") else dominant
+    if args.path == "two_stage":
+        kname = {"dispatch": "rank_copy+expand", "combine": "combine_partial+reduce"}[dominant]
 
     def roof(n):
         a = alg[n] / (per_launch_ms[n] * 1e-3) / 1e9

@@ -24,7 +24,10 @@
 namespace ep {
 namespace {
 
-constexpr int kDispatchWarps = 8;  // warps (= tokens) per block
+#ifndef EP_DISPATCH_WARPS
+#define EP_DISPATCH_WARPS 8
+#endif
+constexpr int kDispatchWarps = EP_DISPATCH_WARPS;  // warps per block
 constexpr int kRowRegs = 8;        // destination rows held in registers per pass
 
 template <int U>

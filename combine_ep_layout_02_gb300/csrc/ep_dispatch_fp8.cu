@@ -7,13 +7,16 @@
 // every code and scale written once: T*H*2 read + T*k*(H + H/32) written.
 #include "ep_internal.cuh"
 
+#ifndef EP_FP8_WARPS
+#define EP_FP8_WARPS 8  // warps per block
+#endif
 #ifndef EP_FP8_MIN_BLOCKS
 #define EP_FP8_MIN_BLOCKS 0  // >0: resident blocks per SM the FP8 kernel is compiled for
 #endif
 #if EP_FP8_MIN_BLOCKS > 0
-#define EP_FP8_BOUNDS __launch_bounds__(256, EP_FP8_MIN_BLOCKS)
+#define EP_FP8_BOUNDS __launch_bounds__(EP_FP8_WARPS * 32, EP_FP8_MIN_BLOCKS)
 #else
-#define EP_FP8_BOUNDS __launch_bounds__(256)
+#define EP_FP8_BOUNDS __launch_bounds__(EP_FP8_WARPS * 32)
 #endif
 #ifndef EP_FP8_U
 #define EP_FP8_U 2  // 512-channel groups per FP8 iteration (loads issued together)
@@ -25,7 +28,7 @@
 namespace ep {
 namespace {
 
-constexpr int kDispatchWarps = 8;  // warps (= tokens) per block
+constexpr int kDispatchWarps = EP_FP8_WARPS;  // warps per block
 constexpr int kRowRegs = 8;        // destination rows held in registers per pass
 
 // FP8: each lane owns 16 consecutive channels (two 16-byte loads, one
@@ -68,7 +71,6 @@ __device__ __forceinline__ Fp8Group quantize16(const uint4& a, const uint4& b) {
     return g;
 }
 
-static_assert(kDispatchWarps * 32 == 256, "EP_FP8_BOUNDS assumes 256-thread blocks");
 __global__ void EP_FP8_BOUNDS
 dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k, int S,
                     int64_t slice_ch, const int32_t* __restrict__ dst_row,
