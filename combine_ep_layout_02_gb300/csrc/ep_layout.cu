@@ -211,7 +211,9 @@ __device__ __forceinline__ unsigned warp_peers(bool valid, int key, int key_bits
 }
 
 // Exclusive scan of in[0..E) (shared) into s_off[0..E] by one block of NT
-// threads; s_warp holds NT/32 ints.  Ends with the block synchronised.
+// threads (NT <= 1024); s_warp holds NT/32 ints.  Two barriers: each warp
+// adds up the totals of the warps before it itself.  Ends with the block
+// synchronised.
 template <int NT>
 __device__ void block_exclusive_scan(const int32_t* in, int E, int32_t* s_off, int32_t* s_warp) {
     const int lane = threadIdx.x & 31;
@@ -229,19 +231,11 @@ __device__ void block_exclusive_scan(const int32_t* in, int E, int32_t* s_off, i
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        const int v = lane < NT / 32 ? s_warp[lane] : 0;
-        int wi = v;
+    int base = lane < warp ? s_warp[lane] : 0;  // warps before this one
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int nb = __shfl_up_sync(kFullMask, wi, o);
-            if (lane >= o) wi += nb;
-        }
-        if (lane < NT / 32) s_warp[lane] = wi - v;  // exclusive warp offsets
-        if (lane == NT / 32 - 1) s_off[E] = wi;       // grand total
-    }
-    __syncthreads();
-    int run = s_warp[warp] + incl - local;
+    for (int o = 16; o > 0; o >>= 1) base += __shfl_xor_sync(kFullMask, base, o);
+    int run = base + incl - local;
+    if (threadIdx.x == NT - 1) s_off[E] = base + incl;  // grand total
     for (int i = 0; i < per; ++i) {
         if (e0 + i < E) {
             s_off[e0 + i] = run;
@@ -288,7 +282,7 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     for (int q = 0; q < kPer; ++q) {
         const int e = threadIdx.x + q * kLayoutThreads;
         if (e < E) {
-            s_tot[e] = (cnt_v[q] + align - 1) / align * align;  // padded segment length
+            s_tot[e] = align > 1 ? (cnt_v[q] + align - 1) / align * align : cnt_v[q];  // padded length
             s_base[e] = base_v[q];
         }
     }
@@ -499,7 +493,7 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     for (int e = threadIdx.x; e < E; e += NT) {
         const int c = s_tot[e];
         expert_counts[e] = c;
-        s_tot[e] = (c + align - 1) / align * align;  // padded segment length
+        if (align > 1) s_tot[e] = (c + align - 1) / align * align;  // padded segment length
     }
     __syncthreads();
     block_exclusive_scan<NT>(s_tot, E, s_off, s_warp);
@@ -582,7 +576,7 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
             total += v;
         }
         s_base[e] = before;
-        s_tot[e] = (total + align - 1) / align * align;  // padded segment length
+        s_tot[e] = align > 1 ? (total + align - 1) / align * align : total;  // padded length
         if (b == 0) expert_counts[e] = total;
     }
     if (b == 0 && rank_token_counts)
