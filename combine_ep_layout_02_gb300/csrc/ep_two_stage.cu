@@ -139,7 +139,8 @@ __device__ __forceinline__ uint32_t ld_row_vec<uint32_t>(const uint32_t* p) { re
 
 template <typename V>
 __device__ __forceinline__ void expand_row(const V* __restrict__ src, V* __restrict__ dst_base,
-                                           int64_t nvec, int k, int my_row, int lane) {
+                                           int64_t nvec, int64_t vb, int64_t ve, int k,
+                                           int my_row, int lane) {
     constexpr int U = 4;
     for (int j0 = 0; j0 < k; j0 += 8) {
         V* dst[8];
@@ -148,12 +149,12 @@ __device__ __forceinline__ void expand_row(const V* __restrict__ src, V* __restr
             const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
             dst[jj] = (j0 + jj < k && r >= 0) ? dst_base + (int64_t)r * nvec : nullptr;
         }
-        for (int64_t v0 = 0; v0 < nvec; v0 += 32 * U) {
+        for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
             V buf[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + u * 32 + lane;
-                if (v < nvec) buf[u] = ld_row_vec<V>(src + v);
+                if (v < ve) buf[u] = ld_row_vec<V>(src + v);
             }
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
@@ -161,36 +162,43 @@ __device__ __forceinline__ void expand_row(const V* __restrict__ src, V* __restr
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t v = v0 + u * 32 + lane;
-                    if (v < nvec) dst[jj][v] = buf[u];
+                    if (v < ve) dst[jj][v] = buf[u];
                 }
             }
         }
     }
 }
 
-// One warp per rank row: copies rank row i of up to two arrays (the payload
-// rows a, and optionally the scale rows b) to the expert rows of its pairs.
+// One warp per rank row (per column slice of it when there are few rows, as
+// for the single-stage row kernels): copies rank row i of up to two arrays
+// (the payload rows a, sliced, and optionally the scale rows b, copied whole
+// by the first slice's warp) to the expert rows of its pairs.
 template <typename VA, typename VB>
 __global__ void __launch_bounds__(kWarps * 32)
-expand_kernel(const VA* __restrict__ a_src, VA* __restrict__ a_dst, int64_t a_nvec,
-              const VB* __restrict__ b_src, VB* __restrict__ b_dst, int64_t b_nvec,
-              const int32_t* __restrict__ rank_offsets, int R, int64_t cap,
+expand_kernel(const VA* __restrict__ a_src, VA* __restrict__ a_dst, int64_t a_nvec, int S,
+              int64_t slice, const VB* __restrict__ b_src, VB* __restrict__ b_dst,
+              int64_t b_nvec, const int32_t* __restrict__ rank_offsets, int R, int64_t cap,
               const int32_t* __restrict__ rank_row_token,
               const int32_t* __restrict__ pair_rank_row, const int32_t* __restrict__ dst_row,
               int64_t T, int k, int64_t rows, uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t i = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t g = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t i = g / S;
     if (i >= live_rank_rows(rank_offsets, R, cap, status)) return;  // warp-uniform
+    const int64_t sl = g - i * S;
+    const int64_t vb = sl * slice;
+    const int64_t ve = vb + slice < a_nvec ? vb + slice : a_nvec;
     const int64_t t = __ldg(rank_row_token + i);
     if (t < 0 || t >= T) {
         if (lane == 0 && status) atomicOr(status, EP_FLAG_BAD_ROW);
         return;
     }
     const int my_row = rank_row_pair(i, t, k, pair_rank_row, dst_row, rows, status);
-    expand_row<VA>(a_src + i * a_nvec, a_dst, a_nvec, k, my_row, lane);
-    if (b_src != nullptr) expand_row<VB>(b_src + i * b_nvec, b_dst, b_nvec, k, my_row, lane);
+    expand_row<VA>(a_src + i * a_nvec, a_dst, a_nvec, vb, ve, k, my_row, lane);
+    if (b_src != nullptr && sl == 0)
+        expand_row<VB>(b_src + i * b_nvec, b_dst, b_nvec, 0, b_nvec, k, my_row, lane);
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
@@ -199,13 +207,16 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
                        const int32_t* __restrict__ pair_rank_row,
                        const int32_t* __restrict__ rank_row_token,
                        const int32_t* __restrict__ rank_offsets, int R, int64_t cap, int64_t T,
-                       int64_t nvec, int k, uint4* __restrict__ partial,
+                       int64_t nvec, int k, int S, int64_t slice, uint4* __restrict__ partial,
                        uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t i = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t g = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t i = g / S;
     if (i >= live_rank_rows(rank_offsets, R, cap, status)) return;
+    const int64_t vb = (g - i * S) * slice;  // this warp's column slice [vb, ve)
+    const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
     const int64_t t = __ldg(rank_row_token + i);
     if (t < 0 || t >= T) {
         if (lane == 0 && status) atomicOr(status, EP_FLAG_BAD_ROW);
@@ -214,7 +225,7 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
     const int my_row = rank_row_pair(i, t, k, pair_rank_row, dst_row, rows, status);
     const float my_w = lane < k ? __ldg(topk_w + t * k + lane) : 0.0f;
     uint4* out_row = partial + i * nvec;
-    for (int64_t v0 = 0; v0 < nvec; v0 += 64) {  // two 16-byte vectors per lane
+    for (int64_t v0 = vb; v0 < ve; v0 += 64) {  // two 16-byte vectors per lane
         float acc[2][8];
 #pragma unroll
         for (int u = 0; u < 2; ++u)
@@ -228,7 +239,7 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int64_t v = v0 + u * 32 + lane;
-                if (v >= nvec) continue;
+                if (v >= ve) continue;
                 const uint4 b = ld_stream_v4(src + v);
                 const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -241,7 +252,7 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int64_t v = v0 + u * 32 + lane;
-            if (v < nvec) {
+            if (v < ve) {
                 uint4 o;
                 o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
                 o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
@@ -256,12 +267,16 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
 __global__ void __launch_bounds__(kWarps * 32)
 combine_reduce_kernel(const uint4* __restrict__ partial, int64_t cap,
                       const int32_t* __restrict__ rank_dst_row, int64_t T, int64_t nvec, int k,
-                      uint4* __restrict__ out, uint32_t* __restrict__ status) {
+                      int S, int64_t slice, uint4* __restrict__ out,
+                      uint32_t* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t g = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t t = g / S;
     if (t >= T) return;
+    const int64_t vb = (g - t * S) * slice;  // this warp's column slice [vb, ve)
+    const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
     int my_row = -1;
     bool bad = false;
     if (lane < k) {
@@ -273,7 +288,7 @@ combine_reduce_kernel(const uint4* __restrict__ partial, int64_t cap,
     }
     warp_flag(status, bad, EP_FLAG_BAD_ROW);
     uint4* out_row = out + t * nvec;
-    for (int64_t v0 = 0; v0 < nvec; v0 += 64) {
+    for (int64_t v0 = vb; v0 < ve; v0 += 64) {
         float acc[2][8];
 #pragma unroll
         for (int u = 0; u < 2; ++u)
@@ -286,7 +301,7 @@ combine_reduce_kernel(const uint4* __restrict__ partial, int64_t cap,
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int64_t v = v0 + u * 32 + lane;
-                if (v >= nvec) continue;
+                if (v >= ve) continue;
                 const uint4 b = ld_stream_v4(src + v);
                 const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -299,7 +314,7 @@ combine_reduce_kernel(const uint4* __restrict__ partial, int64_t cap,
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int64_t v = v0 + u * 32 + lane;
-            if (v < nvec) {
+            if (v < ve) {
                 uint4 o;
                 o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
                 o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
@@ -349,11 +364,12 @@ cudaError_t launch_expand(const void* rank_buf, const int32_t* rank_offsets, int
                           const int32_t* dst_row, int64_t T, int64_t H, int k, void* recv,
                           int64_t rows, uint32_t* status, cudaStream_t stream) {
     if (cap == 0 || T == 0) return cudaSuccess;
-    return launch_pdl(expand_kernel<uint4, uint4>, dim3(blocks_for(cap, kWarps)),
+    const RowSlices sl = row_slices(cap, H / 8);
+    return launch_pdl(expand_kernel<uint4, uint4>, dim3(blocks_for(cap * sl.S, kWarps)),
                       dim3(kWarps * 32), 0, stream, static_cast<const uint4*>(rank_buf),
-                      static_cast<uint4*>(recv), H / 8, (const uint4*)nullptr, (uint4*)nullptr,
-                      (int64_t)0, rank_offsets, R, cap, rank_row_token, pair_rank_row, dst_row, T,
-                      k, rows, status);
+                      static_cast<uint4*>(recv), H / 8, sl.S, sl.slice, (const uint4*)nullptr,
+                      (uint4*)nullptr, (int64_t)0, rank_offsets, R, cap, rank_row_token,
+                      pair_rank_row, dst_row, T, k, rows, status);
 }
 
 cudaError_t launch_expand_fp8(const uint8_t* rank_q, const float* rank_scale,
@@ -363,9 +379,10 @@ cudaError_t launch_expand_fp8(const uint8_t* rank_q, const float* rank_scale,
                               uint8_t* recv_q, float* recv_scale, int64_t rows, uint32_t* status,
                               cudaStream_t stream) {
     if (cap == 0 || T == 0) return cudaSuccess;
-    return launch_pdl(expand_kernel<uint4, uint32_t>, dim3(blocks_for(cap, kWarps)),
+    const RowSlices sl = row_slices(cap, H / 16);
+    return launch_pdl(expand_kernel<uint4, uint32_t>, dim3(blocks_for(cap * sl.S, kWarps)),
                       dim3(kWarps * 32), 0, stream, reinterpret_cast<const uint4*>(rank_q),
-                      reinterpret_cast<uint4*>(recv_q), H / 16,
+                      reinterpret_cast<uint4*>(recv_q), H / 16, sl.S, sl.slice,
                       reinterpret_cast<const uint32_t*>(rank_scale),
                       reinterpret_cast<uint32_t*>(recv_scale), H / 128, rank_offsets, R, cap,
                       rank_row_token, pair_rank_row, dst_row, T, k, rows, status);
@@ -377,19 +394,22 @@ cudaError_t launch_combine_partial(const void* y, int64_t rows, const float* top
                                    int R, int64_t cap, int64_t T, int64_t H, int k, void* partial,
                                    uint32_t* status, cudaStream_t stream) {
     if (cap == 0 || T == 0) return cudaSuccess;
-    return launch_pdl(combine_partial_kernel, dim3(blocks_for(cap, kWarps)), dim3(kWarps * 32), 0,
-                      stream, static_cast<const uint4*>(y), rows, topk_w, dst_row, pair_rank_row,
-                      rank_row_token, rank_offsets, R, cap, T, H / 8, k,
-                      static_cast<uint4*>(partial), status);
+    const RowSlices sl = row_slices(cap, H / 8);
+    return launch_pdl(combine_partial_kernel, dim3(blocks_for(cap * sl.S, kWarps)),
+                      dim3(kWarps * 32), 0, stream, static_cast<const uint4*>(y), rows, topk_w,
+                      dst_row, pair_rank_row, rank_row_token, rank_offsets, R, cap, T, H / 8, k,
+                      sl.S, sl.slice, static_cast<uint4*>(partial), status);
 }
 
 cudaError_t launch_combine_reduce(const void* partial, int64_t cap, const int32_t* rank_dst_row,
                                   int64_t T, int64_t H, int k, void* out, uint32_t* status,
                                   cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    return launch_pdl(combine_reduce_kernel, dim3(blocks_for(T, kWarps)), dim3(kWarps * 32), 0,
-                      stream, static_cast<const uint4*>(partial), cap, rank_dst_row, T, H / 8, k,
-                      static_cast<uint4*>(out), status);
+    const RowSlices sl = row_slices(T, H / 8);
+    return launch_pdl(combine_reduce_kernel, dim3(blocks_for(T * sl.S, kWarps)),
+                      dim3(kWarps * 32), 0, stream, static_cast<const uint4*>(partial), cap,
+                      rank_dst_row, T, H / 8, k, sl.S, sl.slice, static_cast<uint4*>(out),
+                      status);
 }
 
 }  // namespace ep

@@ -52,7 +52,8 @@ def test_rank_layout_random(T, k, E, R):
 
 
 @pytest.mark.parametrize("name,T,H", [("small", 128, 2048), ("prefill", 3000, 1024),
-                                      ("decode_fp8", 700, 512), ("masked", 2048, 256)])
+                                      ("decode_fp8", 700, 512), ("masked", 2048, 256),
+                                      ("prefill", 20, 1336), ("small", 3, 7168)])
 def test_two_stage_path_matches_single_stage(name, T, H):
     wl = W.WORKLOADS[name].scaled(T=T, H=H, capacity=min(W.WORKLOADS[name].capacity, T) or None)
     x = W.hidden_states(wl, device=DEV)
@@ -104,7 +105,8 @@ def test_two_stage_full_size_prefill():
     assert int(rl.rank_offsets[-1]) == int(lay.rank_token_counts.sum())
 
 
-@pytest.mark.parametrize("name,T,H", [("decode_fp8", 2048, 7168), ("prefill_fp8", 1500, 384)])
+@pytest.mark.parametrize("name,T,H", [("decode_fp8", 2048, 7168), ("prefill_fp8", 1500, 384),
+                                      ("decode_fp8", 40, 7168), ("prefill_fp8", 9, 1664)])
 def test_two_stage_fp8_matches_direct_and_oracle(name, T, H):
     wl = W.WORKLOADS[name].scaled(T=T, H=H, capacity=min(W.WORKLOADS[name].capacity, T) or None)
     x = W.hidden_states(wl, device=DEV)
