@@ -157,8 +157,12 @@ def measured_peak():
 
 
 def source_hash(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel's source file and the device helpers it includes."""
+    h = hashlib.sha256()
+    for path in (rel, "combine_ep_layout_02_gb300/csrc/ep_internal.cuh"):
+        with open(os.path.join(ROOT, path), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel, workload):

@@ -28,58 +28,6 @@ namespace {
 #endif
 
 constexpr int kCombineWarps = EP_COMBINE_WARPS;
-constexpr int kRowBatch = 8;  // rows whose loads are issued together
-
-// Accumulate one batch of up to kRowBatch rows into acc for the U column
-// groups starting at v0 (vectors below vend only): all loads first, then the
-// FMAs in j order.
-template <int U>
-__device__ __forceinline__ void accumulate_batch(const uint4* const (&src)[kRowBatch],
-                                                 const float (&wj)[kRowBatch], int64_t v0,
-                                                 int64_t vend, int lane, float (&acc)[U][8]) {
-    uint4 buf[kRowBatch][U];
-#pragma unroll
-    for (int jj = 0; jj < kRowBatch; ++jj) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * 32 + lane;
-            buf[jj][u] = make_uint4(0, 0, 0, 0);
-            if (src[jj] != nullptr && v < vend) buf[jj][u] = ld_stream_v4(src[jj] + v);
-        }
-    }
-#pragma unroll
-    for (int jj = 0; jj < kRowBatch; ++jj) {
-        if (src[jj] == nullptr) continue;  // warp-uniform: skipped pairs add nothing
-        const float w = wj[jj];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t wv[4] = {buf[jj][u].x, buf[jj][u].y, buf[jj][u].z, buf[jj][u].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[u][2 * i] = __fmaf_rn(w, bf16lo_to_f32(wv[i]), acc[u][2 * i]);
-                acc[u][2 * i + 1] = __fmaf_rn(w, bf16hi_to_f32(wv[i]), acc[u][2 * i + 1]);
-            }
-        }
-    }
-}
-
-template <int U>
-__device__ __forceinline__ void store_bf16(uint4* out_row, int64_t v0, int64_t vend, int lane,
-                                           const float (&acc)[U][8]) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int64_t v = v0 + u * 32 + lane;
-        if (v < vend) {
-            uint4 o;
-            o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
-            o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
-            o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
-            o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
-            st_v4(out_row + v, o);
-        }
-    }
-}
-
 template <int U>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
@@ -90,7 +38,7 @@ combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-    const int64_t t = g / S;
+    const int64_t t = slice_row(g, S);
     if (t >= T) return;  // warp-uniform
     const int64_t vb = (g - t * S) * slice;          // this warp's column slice [vb, ve)
     const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
@@ -107,50 +55,7 @@ combine_kernel(const uint4* __restrict__ y, const float* __restrict__ topk_w,
         }
     }
     warp_flag(status, bad, EP_FLAG_BAD_ROW);
-    uint4* out_row = out + t * nvec;
-
-    if (k <= kRowBatch) {
-        // one batch: row pointers and weights stay in registers for the row
-        const uint4* src[kRowBatch];
-        float wj[kRowBatch];
-#pragma unroll
-        for (int jj = 0; jj < kRowBatch; ++jj) {
-            const int r = __shfl_sync(kFullMask, my_row, jj);
-            wj[jj] = __shfl_sync(kFullMask, my_w, jj);
-            src[jj] = (jj < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
-        }
-        for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
-            float acc[U][8];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-            accumulate_batch<U>(src, wj, v0, ve, lane, acc);
-            store_bf16<U>(out_row, v0, ve, lane, acc);
-        }
-        return;
-    }
-    // k > kRowBatch: batches of kRowBatch rows inside each column group
-    for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
-        float acc[U][8];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-        for (int j0 = 0; j0 < k; j0 += kRowBatch) {
-            const uint4* src[kRowBatch];
-            float wj[kRowBatch];
-#pragma unroll
-            for (int jj = 0; jj < kRowBatch; ++jj) {
-                const int j = j0 + jj;
-                const int r = __shfl_sync(kFullMask, my_row, j & 31);
-                wj[jj] = __shfl_sync(kFullMask, my_w, j & 31);
-                src[jj] = (j < k && r >= 0) ? y + (int64_t)r * nvec : nullptr;
-            }
-            accumulate_batch<U>(src, wj, v0, ve, lane, acc);
-        }
-        store_bf16<U>(out_row, v0, ve, lane, acc);
-    }
+    reduce_rows<U>(y, nvec, k, my_row, my_w, vb, ve, out + t * nvec, lane);
 }
 
 // The same reduction with 32-byte accesses: each lane owns 16 channels (one

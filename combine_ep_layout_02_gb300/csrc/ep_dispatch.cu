@@ -39,7 +39,7 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
-    const int64_t t = g / S;
+    const int64_t t = slice_row(g, S);
     if (t >= T) return;  // warp-uniform
     const int64_t vb = (g - t * S) * slice;          // this warp's column slice [vb, ve)
     const int64_t ve = vb + slice < nvec ? vb + slice : nvec;

@@ -81,7 +81,7 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
-    const int64_t t = g / S;
+    const int64_t t = slice_row(g, S);
     if (t >= T) return;
     // this warp's channels [cb, ce): multiples of 512 (S > 1) or the whole row,
     // so that all 8 lanes of a 128-channel block agree on every bound below

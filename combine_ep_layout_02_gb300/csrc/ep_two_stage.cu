@@ -17,7 +17,10 @@
 //   partial     : one warp per rank row, fp32 FMA chain over those pairs in
 //                 increasing j, rounded to bf16.
 //   reduce      : one warp per token, fp32 sum of its rank rows' partials in
-//                 increasing j of their first pair, rounded to bf16.
+//                 increasing j of their first pair, rounded to bf16 (the same
+//                 reducer with unit weights).
+// With few rows each row is split into column slices, one warp each, as in
+// the single-stage row kernels.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -185,7 +188,7 @@ expand_kernel(const VA* __restrict__ a_src, VA* __restrict__ a_dst, int64_t a_nv
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int64_t i = g / S;
+    const int64_t i = slice_row(g, S);
     if (i >= live_rank_rows(rank_offsets, R, cap, status)) return;  // warp-uniform
     const int64_t sl = g - i * S;
     const int64_t vb = sl * slice;
@@ -201,6 +204,10 @@ expand_kernel(const VA* __restrict__ a_src, VA* __restrict__ a_dst, int64_t a_nv
         expand_row<VB>(b_src + i * b_nvec, b_dst, b_nvec, 0, b_nvec, k, my_row, lane);
 }
 
+// SLICED: rows split into column slices (few rows).  The unsliced instance
+// keeps the loop bounds plain: with the slice bounds live, ptxas spilled in
+// the unrolled pair loop and the kernel lost 2.7 % at prefill.
+template <bool SLICED>
 __global__ void __launch_bounds__(kWarps * 32)
 combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* __restrict__ topk_w,
                        const int32_t* __restrict__ dst_row,
@@ -213,10 +220,10 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int64_t i = g / S;
+    const int64_t i = SLICED ? slice_row(g, S) : g;
     if (i >= live_rank_rows(rank_offsets, R, cap, status)) return;
-    const int64_t vb = (g - i * S) * slice;  // this warp's column slice [vb, ve)
-    const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
+    const int64_t vb = SLICED ? (g - i * S) * slice : 0;  // this warp's column slice [vb, ve)
+    const int64_t ve = SLICED ? (vb + slice < nvec ? vb + slice : nvec) : nvec;
     const int64_t t = __ldg(rank_row_token + i);
     if (t < 0 || t >= T) {
         if (lane == 0 && status) atomicOr(status, EP_FLAG_BAD_ROW);
@@ -224,6 +231,10 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
     }
     const int my_row = rank_row_pair(i, t, k, pair_rank_row, dst_row, rows, status);
     const float my_w = lane < k ? __ldg(topk_w + t * k + lane) : 0.0f;
+    // a rank row holds few of the token's pairs (1.8 on average at 8 of 256
+    // experts over 16 ranks), so this walks the pairs one at a time: at 40
+    // registers it keeps 48 warps per SM in flight, which beats batching the
+    // loads of all k slots (121 registers, 29 % slower at prefill)
     uint4* out_row = partial + i * nvec;
     for (int64_t v0 = vb; v0 < ve; v0 += 64) {  // two 16-byte vectors per lane
         float acc[2][8];
@@ -249,18 +260,7 @@ combine_partial_kernel(const uint4* __restrict__ y, int64_t rows, const float* _
                 }
             }
         }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t v = v0 + u * 32 + lane;
-            if (v < ve) {
-                uint4 o;
-                o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
-                o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
-                o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
-                o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
-                st_v4(out_row + v, o);
-            }
-        }
+        store_bf16<2>(out_row, v0, ve, lane, acc);
     }
 }
 
@@ -273,7 +273,7 @@ combine_reduce_kernel(const uint4* __restrict__ partial, int64_t cap,
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int64_t t = g / S;
+    const int64_t t = slice_row(g, S);
     if (t >= T) return;
     const int64_t vb = (g - t * S) * slice;  // this warp's column slice [vb, ve)
     const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
@@ -287,43 +287,7 @@ combine_reduce_kernel(const uint4* __restrict__ partial, int64_t cap,
         }
     }
     warp_flag(status, bad, EP_FLAG_BAD_ROW);
-    uint4* out_row = out + t * nvec;
-    for (int64_t v0 = vb; v0 < ve; v0 += 64) {
-        float acc[2][8];
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int r = __shfl_sync(kFullMask, my_row, j);
-            if (r < 0) continue;  // warp-uniform
-            const uint4* src = partial + (int64_t)r * nvec;
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int64_t v = v0 + u * 32 + lane;
-                if (v >= ve) continue;
-                const uint4 b = ld_stream_v4(src + v);
-                const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[u][2 * q] = __fadd_rn(acc[u][2 * q], bf16lo_to_f32(wv[q]));
-                    acc[u][2 * q + 1] = __fadd_rn(acc[u][2 * q + 1], bf16hi_to_f32(wv[q]));
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t v = v0 + u * 32 + lane;
-            if (v < ve) {
-                uint4 o;
-                o.x = pack_bf16x2_rn(acc[u][0], acc[u][1]);
-                o.y = pack_bf16x2_rn(acc[u][2], acc[u][3]);
-                o.z = pack_bf16x2_rn(acc[u][4], acc[u][5]);
-                o.w = pack_bf16x2_rn(acc[u][6], acc[u][7]);
-                st_v4(out_row + v, o);
-            }
-        }
-    }
+    reduce_rows<2>(partial, nvec, k, my_row, 1.0f, vb, ve, out + t * nvec, lane);
 }
 
 inline unsigned blocks_for(int64_t n, int per_block) {
@@ -395,10 +359,11 @@ cudaError_t launch_combine_partial(const void* y, int64_t rows, const float* top
                                    uint32_t* status, cudaStream_t stream) {
     if (cap == 0 || T == 0) return cudaSuccess;
     const RowSlices sl = row_slices(cap, H / 8);
-    return launch_pdl(combine_partial_kernel, dim3(blocks_for(cap * sl.S, kWarps)),
-                      dim3(kWarps * 32), 0, stream, static_cast<const uint4*>(y), rows, topk_w,
-                      dst_row, pair_rank_row, rank_row_token, rank_offsets, R, cap, T, H / 8, k,
-                      sl.S, sl.slice, static_cast<uint4*>(partial), status);
+    return launch_pdl(sl.S > 1 ? combine_partial_kernel<true> : combine_partial_kernel<false>,
+                      dim3(blocks_for(cap * sl.S, kWarps)), dim3(kWarps * 32), 0, stream,
+                      static_cast<const uint4*>(y), rows, topk_w, dst_row, pair_rank_row,
+                      rank_row_token, rank_offsets, R, cap, T, H / 8, k, sl.S, sl.slice,
+                      static_cast<uint4*>(partial), status);
 }
 
 cudaError_t launch_combine_reduce(const void* partial, int64_t cap, const int32_t* rank_dst_row,

@@ -14,7 +14,10 @@ The five named workloads follow the shapes the pages measure:
     layout included                                     -> ``prefill``, ``prefill_fp8``
 Routes are uniform or Zipf-skewed instead of the PR's perfectly balanced
 ``(t*17 + j*31 + seed) mod 256`` route, which is kept as an extra test input
-(``balanced_route``).
+(``balanced_route``).  A sixth workload, ``prefill_grouped``, limits each
+token to 4 of 8 virtual ranks (group-limited routing, the reason DeepEP-style
+dispatch sends one copy per destination and expands it there), so that the
+two-stage path has real per-rank deduplication to exploit.
 
 Seeds: workload ``i`` (1-based, in the order above) uses seed ``0xEB00 + i``;
 each quantity has its own sub-stream.  Random draws use ``torch.Generator``
@@ -39,8 +42,9 @@ class Workload:
     kind: str              # "contiguous" | "masked"
     capacity: int          # rows per expert in the masked layout (0 for contiguous)
     payload: str           # "bf16" | "fp8"
-    route: str             # "uniform" | "zipf" | "balanced"
+    route: str             # "uniform" | "zipf" | "balanced" | "grouped"
     zipf_s: float = 0.0
+    groups_per_token: int = 0   # "grouped": virtual ranks a token's experts may span
     outlier_frac: float = 0.0   # fraction of channels scaled x100
     expert_out: str = "independent"  # "independent" | "recv" | "scaled_recv"
     seed: int = 0
@@ -83,6 +87,11 @@ WORKLOADS = {
                             kind="contiguous", capacity=0, payload="fp8", route="zipf",
                             zipf_s=1.2, outlier_frac=0.01, seed=0xEB05,
                             notes="32 virtual ranks x 4096 tokens; Zipf(1.2); 1% outlier channels"),
+    "prefill_grouped": Workload("prefill_grouped", T=65536, H=7168, E=256, k=8, R=8,
+                                kind="contiguous", capacity=0, payload="bf16", route="grouped",
+                                groups_per_token=4, expert_out="recv", seed=0xEB06,
+                                notes="8 virtual ranks x 32 experts; each token's 8 experts "
+                                      "within 4 ranks (at least 2 pairs per rank copy)"),
 }
 
 _STREAMS = {"x": 1, "route": 2, "logits": 3, "y": 4, "scale": 5, "outliers": 6}
@@ -129,7 +138,11 @@ def route(wl, device="cpu", chunk_rows=16384):
     uniform: a uniformly random k-subset in random order (top-k of i.i.d.
     uniform keys).  zipf: successive draws without replacement with expert
     popularity p_e proportional to (e+1)^-s (expert 0 hottest), via the
-    Gumbel-top-k construction: top-k of log p_e + Gumbel noise."""
+    Gumbel-top-k construction: top-k of log p_e + Gumbel noise.  grouped:
+    first a uniformly random set of ``groups_per_token`` of the R virtual
+    ranks (top of i.i.d. uniform rank keys), then a uniformly random k-subset
+    of those ranks' experts (their uniform keys; the other experts' keys are
+    set below every draw)."""
     if wl.route == "balanced":
         return balanced_route(wl.T, wl.k, wl.E, wl.seed).to(device)
     g = _gen(wl.seed, "route", device)
@@ -142,6 +155,14 @@ def route(wl, device="cpu", chunk_rows=16384):
         u = torch.rand(r1 - r0, wl.E, generator=g, device=device, dtype=torch.float32)
         if wl.route == "uniform":
             keys = u
+        elif wl.route == "grouped":
+            per = wl.E // wl.R
+            if wl.groups_per_token * per < wl.k:
+                raise ValueError("grouped route: the chosen ranks hold fewer than k experts")
+            ru = torch.rand(r1 - r0, wl.R, generator=g, device=device, dtype=torch.float32)
+            chosen = torch.zeros(r1 - r0, wl.R, dtype=torch.bool, device=device)
+            chosen.scatter_(1, torch.topk(ru, wl.groups_per_token, dim=1).indices, True)
+            keys = torch.where(chosen.repeat_interleave(per, dim=1), u, torch.full_like(u, -1.0))
         elif wl.route == "zipf":
             u = u.clamp_min(torch.finfo(torch.float32).tiny)
             keys = logp.view(1, -1) - torch.log(-torch.log(u))

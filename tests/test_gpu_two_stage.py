@@ -53,7 +53,8 @@ def test_rank_layout_random(T, k, E, R):
 
 @pytest.mark.parametrize("name,T,H", [("small", 128, 2048), ("prefill", 3000, 1024),
                                       ("decode_fp8", 700, 512), ("masked", 2048, 256),
-                                      ("prefill", 20, 1336), ("small", 3, 7168)])
+                                      ("prefill", 20, 1336), ("small", 3, 7168),
+                                      ("prefill_grouped", 3000, 1024)])
 def test_two_stage_path_matches_single_stage(name, T, H):
     wl = W.WORKLOADS[name].scaled(T=T, H=H, capacity=min(W.WORKLOADS[name].capacity, T) or None)
     x = W.hidden_states(wl, device=DEV)
@@ -83,6 +84,8 @@ def test_two_stage_path_matches_single_stage(name, T, H):
     assert np.array_equal(_bits(out), rout)
     _, r64, absum = oracle.combine_f64(_bits(y), w.cpu().numpy(), dst)
     assert np.all(np.abs(_f(_bits(out)) - r64) <= 2.0 ** -8 * np.abs(r64) + 2.0 ** -8 * absum + 1e-30)
+    if wl.route == "grouped":             # at most groups_per_token rank copies per token
+        assert n <= wl.T * wl.groups_per_token
 
 
 def test_two_stage_full_size_prefill():

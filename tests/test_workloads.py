@@ -69,3 +69,19 @@ def test_logical_bytes_formula():
     f = W.WORKLOADS["prefill_fp8"]
     d, c = f.logical_bytes()
     assert d == f.T * f.k * (f.H + 4 * f.H // 128) and c == f.T * f.k * f.H * 2
+
+
+def test_grouped_route_spans_few_ranks():
+    wl = W.WORKLOADS["prefill_grouped"].scaled(T=4000)
+    idx = W.route(wl).numpy()
+    per = wl.E // wl.R
+    ranks = idx // per
+    spans = np.array([len(set(r)) for r in ranks.tolist()])
+    assert spans.max() <= wl.groups_per_token                     # at most 4 of the 8 ranks
+    assert spans.min() >= -(-wl.k // per)                          # k experts need this many ranks
+    assert all(len(set(r)) == wl.k for r in idx.tolist())          # distinct experts
+    # every rank and expert is used, roughly evenly (uniform within the chosen ranks)
+    cnt = np.bincount(idx.reshape(-1), minlength=wl.E)
+    assert cnt.min() > 0 and cnt.max() / cnt.min() < 1.6
+    rc = np.bincount(ranks.reshape(-1), minlength=wl.R)
+    assert rc.max() / rc.min() < 1.2
