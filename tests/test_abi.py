@@ -42,6 +42,17 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_binding_constants_match_the_header():
+    from combine_ep_layout_02_gb300 import binding
+    with open(os.path.join(ROOT, "include", "ep.h")) as f:
+        text = f.read()
+    consts = dict(re.findall(r"\b(EP_(?:FLAG|ERR|OK)\w*)\s*=\s*(\d+)u?\b", text))
+    assert {"EP_FLAG_BAD_EXPERT", "EP_FLAG_OVERFLOW", "EP_FLAG_BAD_ROW", "EP_FLAG_TIMEOUT",
+            "EP_ERR_INVALID_ARG", "EP_ERR_ALIGNMENT", "EP_ERR_WORKSPACE", "EP_ERR_CUDA"} <= set(consts)
+    for name, value in consts.items():
+        assert getattr(binding, name) == int(value), name
+
+
 def test_version_and_status_strings(lib):
     assert lib.ep_version() >> 16 == 1
     assert lib.ep_status_string(0) == b"EP_OK"
