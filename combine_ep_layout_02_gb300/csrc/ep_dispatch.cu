@@ -17,6 +17,9 @@
 #ifndef EP_DISPATCH_U
 #define EP_DISPATCH_U 4  // 16-byte vectors per lane in flight per row pass
 #endif
+#ifndef EP_DISPATCH_PREFETCH_MIN_TOKENS
+#define EP_DISPATCH_PREFETCH_MIN_TOKENS 16384  // batches this large use PREFETCH
+#endif
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
 #endif
@@ -30,7 +33,14 @@ namespace {
 constexpr int kDispatchWarps = EP_DISPATCH_WARPS;  // warps per block
 constexpr int kRowRegs = 8;        // destination rows held in registers per pass
 
-template <int U>
+// PREFETCH: the first pass's loads are issued before the destination rows
+// are read.  It costs registers (88 instead of 58: 2 blocks per SM instead of
+// 4), which measured faster for large batches (65,536 tokens x 7168:
+// 1275 -> 1257 us, and 1292 -> 1275 us on a second GB300; the occupancy cap
+// alone gave 1279 us there) but 1-2 % slower at 1,024 to 2,048 tokens and no
+// faster below, so the launcher uses it from EP_DISPATCH_PREFETCH_MIN_TOKENS
+// tokens up.  The same change in the FP8 dispatch measured 0.15 % slower.
+template <int U, bool PREFETCH>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k, int S,
                      int64_t slice, const int32_t* __restrict__ dst_row, uint4* __restrict__ recv,
@@ -43,8 +53,18 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
     if (t >= T) return;  // warp-uniform
     const int64_t vb = (g - t * S) * slice;          // this warp's column slice [vb, ve)
     const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
-    const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const uint4* src = x + t * nvec;
+    // the first pass's loads do not depend on the destination rows: issue
+    // them before the rows are read, so the two latencies overlap
+    uint4 first[U];
+    if (PREFETCH) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = vb + u * 32 + lane;
+            if (v < ve) first[u] = ld_stream_v4(src + v);
+        }
+    }
+    const int my_row = load_dst_row(dst_row, t, k, rows, status);
     // k <= 8 is one pass; larger k re-reads the slice once per 8 destinations
     for (int j0 = 0; j0 < k; j0 += kRowRegs) {
         uint4* dst[kRowRegs];
@@ -55,10 +75,12 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
         }
         for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
             uint4 buf[U];
+            const bool pre = PREFETCH && j0 == 0 && v0 == vb;  // warp-uniform
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + u * 32 + lane;
-                if (v < ve) buf[u] = ld_stream_v4(src + v);
+                if (pre) buf[u] = first[u];
+                else if (v < ve) buf[u] = ld_stream_v4(src + v);
             }
 #pragma unroll
             for (int jj = 0; jj < kRowRegs; ++jj) {
@@ -175,8 +197,11 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
     const int64_t nvec = H / 8;
     const RowSlices sl = row_slices(T, nvec);
     const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
-    return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U>, dim3(grid), dim3(kDispatchWarps * 32), 0,
-                      stream, static_cast<const uint4*>(x), T, nvec, k, sl.S, sl.slice, dst_row,
+    const bool prefetch = T >= EP_DISPATCH_PREFETCH_MIN_TOKENS;
+    return launch_pdl(prefetch ? dispatch_bf16_kernel<EP_DISPATCH_U, true>
+                               : dispatch_bf16_kernel<EP_DISPATCH_U, false>,
+                      dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
+                      static_cast<const uint4*>(x), T, nvec, k, sl.S, sl.slice, dst_row,
                       static_cast<uint4*>(recv), rows, status);
 }
 
