@@ -6,6 +6,8 @@
 // (streaming, no L1 allocation) and writes it to each of the k destination
 // rows, so every input byte is read once and every output byte written once:
 // the HBM floor is T*H*2 read + T*k*H*2 written.
+#include <atomic>
+
 #include "ep_internal.cuh"
 
 #ifndef EP_DISPATCH_BULK
@@ -34,12 +36,11 @@ constexpr int kDispatchWarps = EP_DISPATCH_WARPS;  // warps per block
 constexpr int kRowRegs = 8;        // destination rows held in registers per pass
 
 // PREFETCH: the first pass's loads are issued before the destination rows
-// are read.  It costs registers (88 instead of 58: 2 blocks per SM instead of
-// 4), which measured faster for large batches (65,536 tokens x 7168:
-// 1275 -> 1257 us, and 1292 -> 1275 us on a second GB300; the occupancy cap
-// alone gave 1279 us there) but 1-2 % slower at 1,024 to 2,048 tokens and no
-// faster below, so the launcher uses it from EP_DISPATCH_PREFETCH_MIN_TOKENS
-// tokens up.  The same change in the FP8 dispatch measured 0.15 % slower.
+// are read, so the two latencies overlap (88 registers instead of 58).  Used
+// with the one-block-per-SM launch for large batches (65,536 tokens x 7168:
+// 1275 -> 1257 us at 2 blocks per SM, 1245 us at one); 1-2 % slower at 1,024
+// to 2,048 tokens and no faster below, so smaller batches use the plain
+// instance.  The same change in the FP8 dispatch measured 0.15 % slower.
 template <int U, bool PREFETCH>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k, int S,
@@ -165,6 +166,43 @@ dispatch_bf16_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, uint32_t row
     if (timed_out && lane == 0 && status) atomicOr(status, EP_FLAG_TIMEOUT);
 }
 
+// Dynamic shared memory that admits one block per SM: just over half of an
+// SM's shared memory (0 if the device reports none).  Per device, read once.
+size_t dispatch_occupancy_smem() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int v = cache[dev & 63].load(std::memory_order_relaxed);
+    if (v == 0) {
+        int per_sm = 0, per_block = 0;
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return 0;
+        v = per_sm / 2 + 1024;
+        if (v > per_block) v = -1;  // cannot be enforced this way: no request
+        cache[dev & 63].store(v, std::memory_order_relaxed);
+    }
+    return v > 0 ? (size_t)v : 0;
+}
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes`, once per device.
+template <typename K>
+cudaError_t raise_smem_limit_once(K kernel, size_t bytes) {
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (err != cudaSuccess) return err;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
@@ -197,10 +235,23 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
     const int64_t nvec = H / 8;
     const RowSlices sl = row_slices(T, nvec);
     const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
-    const bool prefetch = T >= EP_DISPATCH_PREFETCH_MIN_TOKENS;
-    return launch_pdl(prefetch ? dispatch_bf16_kernel<EP_DISPATCH_U, true>
-                               : dispatch_bf16_kernel<EP_DISPATCH_U, false>,
-                      dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
+    if (T < EP_DISPATCH_PREFETCH_MIN_TOKENS)
+        return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U, false>, dim3(grid),
+                          dim3(kDispatchWarps * 32), 0, stream, static_cast<const uint4*>(x), T,
+                          nvec, k, sl.S, sl.slice, dst_row, static_cast<uint4*>(recv), rows,
+                          status);
+    // Large batches: at most one 8-warp block per SM.  A write-bound scatter
+    // into k rows per token measured fastest with 8 warps per SM (65,536 x
+    // 7168: 1257 us at 16 warps, 1245 us at 8, 1403 us at 4), which the
+    // block's dynamic shared-memory request enforces (it is not otherwise
+    // used): more than half an SM's shared memory admits one block per SM.
+    auto kern = dispatch_bf16_kernel<EP_DISPATCH_U, true>;
+    const size_t smem = dispatch_occupancy_smem();
+    if (smem > 0) {
+        const cudaError_t e = raise_smem_limit_once(kern, smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(kern, dim3(grid), dim3(kDispatchWarps * 32), smem, stream,
                       static_cast<const uint4*>(x), T, nvec, k, sl.S, sl.slice, dst_row,
                       static_cast<uint4*>(recv), rows, status);
 }
