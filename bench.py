@@ -578,7 +578,9 @@ def run_ours(args, rank, world, local):
                 "frac": frac, "peak_source": peak_src + " (%s)" % (
                     "MEASURED_PEAKS.json hbm_gbs" if peak_src == "measured" else "6.8 TB/s"),
                 "algorithmic_bytes_per_launch": alg[dominant],
-                "traffic": ncu_traffic(kname, wl.name)}
+                # counters were captured on the full-size workload only
+                "traffic": None if (args.tokens or args.seed is not None or args.path != "direct")
+                else ncu_traffic(kname, wl.name)}
     kernels = {}
     step_sum = sum(per_launch_ms.values())
     for n in ("layout", "dispatch", "combine"):
