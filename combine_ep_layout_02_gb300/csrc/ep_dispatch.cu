@@ -5,7 +5,8 @@
 // tokens).  The warp reads its part of the row once in 16-byte vectors
 // (streaming, no L1 allocation) and writes it to each of the k destination
 // rows, so every input byte is read once and every output byte written once:
-// the HBM floor is T*H*2 read + T*k*H*2 written.
+// the HBM floor is T*H*2 read + T*k*H*2 written.  Large batches run at most
+// one 8-warp block per SM, where this write-bound scatter is fastest.
 #include <atomic>
 
 #include "ep_internal.cuh"
