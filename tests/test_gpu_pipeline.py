@@ -22,7 +22,8 @@ def built():
 
 
 @pytest.mark.parametrize("name,T,H,chunk", [("prefill", 3000, 7168, 512), ("masked", 2048, 2048, 2048),
-                                            ("small", 128, 2048, 7), ("prefill", 5, 64, 1)])
+                                            ("small", 128, 2048, 7), ("prefill", 5, 64, 1),
+                                            ("masked", 2048, 1024, 100)])
 def test_roundtrip_matches_device_calls(name, T, H, chunk):
     wl = W.WORKLOADS[name].scaled(T=T, H=H, capacity=min(W.WORKLOADS[name].capacity, T) or None)
     x, idx, w = W.hidden_states(wl), W.route(wl), W.topk_weights(wl)
