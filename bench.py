@@ -75,6 +75,8 @@ def parse():
                     help="never flush L2 (warm-L2 numbers for working sets that fit in L2)")
     ap.add_argument("--layout-only", action="store_true",
                     help="time only the routing layout (20 calls captured in one CUDA graph)")
+    ap.add_argument("--fused", action="store_true",
+                    help="layout + dispatch through ep_layout_dispatch (one launch up to 128 tokens)")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step as one captured CUDA graph (launch-bound small shapes)")
     return ap.parse_args()
@@ -412,6 +414,8 @@ def run_ours(args, rank, world, local):
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    if args.fused and args.path != "direct":
+        raise SystemExit("--fused applies to the direct path")
     if args.path == "two_stage":
         if wl.payload != "bf16":
             raise SystemExit("the two-stage path is BF16 only")
@@ -443,16 +447,28 @@ def run_ours(args, rank, world, local):
             return step_two_stage(ev)
         if ev:
             ev[0].record(stream)
-        ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
-        if ev:
-            ev[1].record(stream)
-        if wl.payload == "fp8":
-            ep.dispatch_fp8(x, lay.dst_row, wl.rows, recv_q=recv_q, recv_scale=recv_s,
-                            status=lay.status)
+        if args.fused:
+            # one call; its time is reported under "layout" + "dispatch" together
+            if wl.payload == "fp8":
+                ep.layout_dispatch(x, idx, wl.E, wl.R, wl.kind, wl.capacity, wl.rows, out=lay,
+                                   workspace=ws, fp8=True, recv_q=recv_q, recv_scale=recv_s)
+            else:
+                ep.layout_dispatch(x, idx, wl.E, wl.R, wl.kind, wl.capacity, wl.rows, out=lay,
+                                   recv=recv, workspace=ws)
+            if ev:
+                ev[1].record(stream)
+                ev[2].record(stream)
         else:
-            ep.dispatch(x, lay.dst_row, wl.rows, recv=recv, status=lay.status)
-        if ev:
-            ev[2].record(stream)
+            ep.layout(idx, wl.E, wl.R, wl.kind, wl.capacity, out=lay, workspace=ws)
+            if ev:
+                ev[1].record(stream)
+            if wl.payload == "fp8":
+                ep.dispatch_fp8(x, lay.dst_row, wl.rows, recv_q=recv_q, recv_scale=recv_s,
+                                status=lay.status)
+            else:
+                ep.dispatch(x, lay.dst_row, wl.rows, recv=recv, status=lay.status)
+            if ev:
+                ev[2].record(stream)
         ep.combine(y, w, lay.dst_row, out=out, status=lay.status)
         if ev:
             ev[3].record(stream)
@@ -462,6 +478,9 @@ def run_ours(args, rank, world, local):
     # layout over keys, finish), the expansion and the final reduce
     lay_launches = 1 if wl.T <= 2048 else 3  # one launch (single block or one cluster) up to 2048 tokens
     launches_per_step = lay_launches + 2
+    fused_one = args.fused and 1 <= wl.T <= 128   # layout and dispatch in one launch
+    if fused_one:
+        launches_per_step = 2
     if args.path == "two_stage":
         launches_per_step = 2 * lay_launches + 2 + 4
 
@@ -552,6 +571,11 @@ def run_ours(args, rank, world, local):
     }
     per_launch_ms = {"layout": lay_ms / args.steps, "dispatch": disp_ms / args.steps,
                      "combine": comb_ms / args.steps}
+    if args.fused:
+        # the fused call is timed as one: its bytes are the layout's and the dispatch's
+        alg = {"layout_dispatch": alg["layout"] + alg["dispatch"], "combine": alg["combine"]}
+        per_launch_ms = {"layout_dispatch": (lay_ms + disp_ms) / args.steps,
+                         "combine": comb_ms / args.steps}
     if args.path == "two_stage":
         # each timed stage is two kernels; nr = rank rows the route fills
         nr = int(rl.rank_offsets[-1])
@@ -562,7 +586,7 @@ def run_ours(args, rank, world, local):
             "combine": (Tk * wl.H * 2 + nr * wl.H * 2 + Tk * 12 + nr * 4)   # rank-local partials
                        + (nr * wl.H * 2 + wl.T * wl.H * 2 + Tk * 4),       # final reduce
         }
-    dominant = max(("dispatch", "combine"), key=lambda n: per_launch_ms[n])
+    dominant = max((n for n in per_launch_ms if n != "layout"), key=lambda n: per_launch_ms[n])
     peak, peak_src = measured_peak()
     kname = "dispatch_fp8" if (dominant == "dispatch" and wl.payload == "fp8") else dominant
     if args.path == "two_stage":
@@ -579,11 +603,12 @@ def run_ours(args, rank, world, local):
                     "MEASURED_PEAKS.json hbm_gbs" if peak_src == "measured" else "6.8 TB/s"),
                 "algorithmic_bytes_per_launch": alg[dominant],
                 # counters were captured on the full-size workload only
-                "traffic": None if (args.tokens or args.seed is not None or args.path != "direct")
+                "traffic": None if (args.tokens or args.seed is not None or args.path != "direct"
+                                    or args.fused)
                 else ncu_traffic(kname, wl.name)}
     kernels = {}
     step_sum = sum(per_launch_ms.values())
-    for n in ("layout", "dispatch", "combine"):
+    for n in per_launch_ms:
         a, f = roof(n)
         kernels[n] = {"us_per_launch": per_launch_ms[n] * 1e3, "alg_bytes": alg[n],
                       "achieved_GBs": a, "frac_of_peak": f, "share": per_launch_ms[n] / step_sum}
@@ -648,7 +673,8 @@ def run_ours(args, rank, world, local):
                        "logical_bytes_per_step": logical,
                        "l2": l2_note,
                        "parallelism": "replicas x%d" % world,
-                       "launch": "cuda graph" if args.graph else "stream (programmatic dependent launch)",
+                       "launch": ("cuda graph" if args.graph else "stream (programmatic dependent launch)")
+                                 + ("; layout+dispatch through ep_layout_dispatch" if args.fused else ""),
                        "path": args.path},
             "roofline": roofline,
             "kernels": kernels,

@@ -65,6 +65,10 @@ def load():
         "ep_combine_partial": ([P, i64, P, P, P, P, P, i32, i64, i64, i64, i32, P, P, P], i32),
         "ep_combine_reduce": ([P, i64, P, i64, i64, i32, P, P, P], i32),
         "ep_dispatch_fp8": ([P, i64, i64, i32, P, P, P, i64, P, P], i32),
+        "ep_layout_dispatch": ([P, i64, i32, i32, i32, i32, i32, P, i64, P, P, P, P, P, i64, P, P,
+                                sz, P], i32),
+        "ep_layout_dispatch_fp8": ([P, i64, i32, i32, i32, i32, i32, P, i64, P, P, P, P, P, P,
+                                    i64, P, P, sz, P], i32),
         "ep_combine": ([P, P, P, i64, i64, i32, i64, P, P, P], i32),
         "ep_status_read": ([P, P, P], i32),
         "ep_pipeline_create": ([i32, ctypes.POINTER(ctypes.c_void_p)], i32),
@@ -144,10 +148,11 @@ def layout(topk_idx, E, R=1, kind="contiguous", capacity=0, *, out=None, workspa
     if alignment != 1:
         if kind != "contiguous":
             raise ValueError("expert alignment applies to the contiguous layout only")
-        code = load().ep_layout_aligned(_ptr(topk_idx), T, k, E, R, alignment,
-                                        _ptr(out.expert_counts), _ptr(out.expert_offsets),
-                                        _ptr(out.dst_row), _ptr(out.rank_token_counts),
-                                        _ptr(out.status), _ptr(workspace), wbytes, _stream(dev))
+        with _on(dev):
+            code = load().ep_layout_aligned(_ptr(topk_idx), T, k, E, R, alignment,
+                                            _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                            _ptr(out.dst_row), _ptr(out.rank_token_counts),
+                                            _ptr(out.status), _ptr(workspace), wbytes, _stream(dev))
         _rc("ep_layout_aligned", code)
         return out
     with _on(dev):
@@ -199,6 +204,61 @@ def dispatch(x, dst_row, rows, recv=None, status=None):
                                   _stream(x.device))
     _rc("ep_dispatch", code)
     return recv
+
+
+def _new_layout(T, k, E, R, with_rank_counts, dev):
+    return LayoutOut(torch.empty(E, dtype=torch.int32, device=dev),
+                     torch.empty(E + 1, dtype=torch.int32, device=dev),
+                     torch.empty(T, k, dtype=torch.int32, device=dev),
+                     torch.empty(R, dtype=torch.int32, device=dev) if with_rank_counts else None,
+                     torch.empty(1, dtype=torch.int32, device=dev))
+
+
+def layout_dispatch(x, topk_idx, E, R=1, kind="contiguous", capacity=0, rows=None, *, out=None,
+                    recv=None, workspace=None, with_rank_counts=True, fp8=False, recv_q=None,
+                    recv_scale=None):
+    """``ep_layout`` then ``ep_dispatch`` (``fp8``: ``ep_dispatch_fp8``) in one
+    call (see ``ep_layout_dispatch``): one kernel launch for up to 128 tokens.
+    Returns (LayoutOut, recv), or (LayoutOut, recv_q, recv_scale) with ``fp8``."""
+    _check_dev("x", x, torch.bfloat16)
+    _check_dev("topk_idx", topk_idx, torch.int32, x.device)
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    dev = x.device
+    if rows is None:
+        rows = T * k if kind == "contiguous" else E * capacity
+    if out is None:
+        out = _new_layout(T, k, E, R, with_rank_counts, dev)
+    need = layout_workspace_bytes(T, k, E, R, out.rank_token_counts is not None)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if fp8:
+        if recv_q is None:
+            recv_q = torch.empty(rows, H, dtype=torch.uint8, device=dev)
+        if recv_scale is None:
+            recv_scale = torch.empty(rows, H // 128, dtype=torch.float32, device=dev)
+        _check_dev("recv_q", recv_q, torch.uint8, dev)
+        _check_dev("recv_scale", recv_scale, torch.float32, dev)
+        with _on(dev):
+            code = load().ep_layout_dispatch_fp8(
+                _ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity, _ptr(x), H,
+                _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.dst_row),
+                _ptr(out.rank_token_counts), _ptr(recv_q), _ptr(recv_scale), rows, _ptr(out.status),
+                _ptr(workspace), wbytes, _stream(dev))
+        _rc("ep_layout_dispatch_fp8", code)
+        return out, recv_q, recv_scale
+    if recv is None:
+        recv = torch.empty(rows, H, dtype=torch.bfloat16, device=dev)
+    _check_dev("recv", recv, torch.bfloat16, dev)
+    with _on(dev):
+        code = load().ep_layout_dispatch(
+            _ptr(topk_idx), T, k, E, R, LAYOUT_KINDS[kind], capacity, _ptr(x), H,
+            _ptr(out.expert_counts), _ptr(out.expert_offsets), _ptr(out.dst_row),
+            _ptr(out.rank_token_counts), _ptr(recv), rows, _ptr(out.status), _ptr(workspace),
+            wbytes, _stream(dev))
+    _rc("ep_layout_dispatch", code)
+    return out, recv
 
 
 def dispatch_fp8(x, dst_row, rows, recv_q=None, recv_scale=None, status=None):

@@ -84,10 +84,11 @@ size_t ep_layout_workspace_bytes(int64_t T, int k, int E, int R, int with_rank_c
 
 namespace {
 
-int layout_checked(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind, int capacity,
-                   int align, int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
-                   int32_t* rank_token_counts, uint32_t* status, void* workspace,
-                   size_t workspace_bytes, void* stream) {
+// The host-side checks of ep_layout (EP_OK when the call may proceed).
+int check_layout_args(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
+                      int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
+                      int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
+                      void* workspace, size_t workspace_bytes) {
     if (T < 0 || k < 1 || k > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS || R < 1 || E % R != 0)
         return EP_ERR_INVALID_ARG;
     if (T > (int64_t)INT32_MAX / k) return EP_ERR_INVALID_ARG;
@@ -105,6 +106,17 @@ int layout_checked(const int32_t* topk_idx, int64_t T, int k, int E, int R, int 
         if (!workspace || workspace_bytes < need) return EP_ERR_WORKSPACE;
         if (!aligned(workspace, 16)) return EP_ERR_ALIGNMENT;
     }
+    return EP_OK;
+}
+
+int layout_checked(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind, int capacity,
+                   int align, int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+                   int32_t* rank_token_counts, uint32_t* status, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    const int rc = check_layout_args(topk_idx, T, k, E, R, kind, capacity, align, expert_counts,
+                                     expert_offsets, dst_row, rank_token_counts, status, workspace,
+                                     workspace_bytes);
+    if (rc != EP_OK) return rc;
     return cuda_status(ep::launch_layout(topk_idx, T, k, E, R, kind, capacity, align,
                                          expert_counts, expert_offsets, dst_row, rank_token_counts,
                                          status, static_cast<int32_t*>(workspace),
@@ -157,6 +169,69 @@ int ep_dispatch_fp8(const void* x, int64_t T, int64_t H, int k, const int32_t* d
         return EP_ERR_ALIGNMENT;
     return cuda_status(ep::launch_dispatch_fp8(x, T, H, k, dst_row, recv_q, recv_scale, rows,
                                                status, as_stream(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// ep_layout then ep_dispatch (fp8: ep_dispatch_fp8) on one status word, as a
+// single launch when the fused kernel covers the shape.
+int layout_dispatch_checked(bool fp8, const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                            int kind, int capacity, const void* x, int64_t H, int32_t* expert_counts,
+                            int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
+                            void* recv, uint8_t* recv_q, float* recv_scale, int64_t rows,
+                            uint32_t* status, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    int rc = check_layout_args(topk_idx, T, k, E, R, kind, capacity, 1, expert_counts,
+                               expert_offsets, dst_row, rank_token_counts, status, workspace,
+                               workspace_bytes);
+    if (rc != EP_OK) return rc;
+    rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (fp8 && H % 128 != 0) return EP_ERR_ALIGNMENT;
+    if (T > 0 && (!x || (fp8 ? ((!recv_q || !recv_scale) && rows > 0) : (!recv && rows > 0))))
+        return EP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(recv_q, 16) || !aligned(recv_scale, 4))
+        return EP_ERR_ALIGNMENT;
+    const cudaError_t e = ep::launch_layout_dispatch(
+        topk_idx, T, k, E, R, kind, capacity, x, H, fp8, expert_counts, expert_offsets, dst_row,
+        rank_token_counts, fp8 ? static_cast<void*>(recv_q) : recv, recv_scale, rows, status,
+        as_stream(stream));
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+    // outside the fused kernel's range: the two launches, same results
+    rc = cuda_status(ep::launch_layout(topk_idx, T, k, E, R, kind, capacity, 1, expert_counts,
+                                       expert_offsets, dst_row, rank_token_counts, status,
+                                       static_cast<int32_t*>(workspace), as_stream(stream)));
+    if (rc != EP_OK || T == 0) return rc;
+    return cuda_status(fp8 ? ep::launch_dispatch_fp8(x, T, H, k, dst_row, recv_q, recv_scale,
+                                                     rows, status, as_stream(stream))
+                           : ep::launch_dispatch_bf16(x, T, H, k, dst_row, recv, rows, status,
+                                                      as_stream(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
+                       int capacity, const void* x, int64_t H, int32_t* expert_counts,
+                       int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
+                       void* recv, int64_t rows, uint32_t* status, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    return layout_dispatch_checked(false, topk_idx, T, k, E, R, kind, capacity, x, H, expert_counts,
+                                   expert_offsets, dst_row, rank_token_counts, recv, nullptr,
+                                   nullptr, rows, status, workspace, workspace_bytes, stream);
+}
+
+int ep_layout_dispatch_fp8(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
+                           int capacity, const void* x, int64_t H, int32_t* expert_counts,
+                           int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
+                           uint8_t* recv_q, float* recv_scale, int64_t rows, uint32_t* status,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    return layout_dispatch_checked(true, topk_idx, T, k, E, R, kind, capacity, x, H, expert_counts,
+                                   expert_offsets, dst_row, rank_token_counts, nullptr, recv_q,
+                                   recv_scale, rows, status, workspace, workspace_bytes, stream);
 }
 
 int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row, int64_t T, int64_t H,

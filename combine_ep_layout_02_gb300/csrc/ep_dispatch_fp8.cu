@@ -32,45 +32,9 @@ constexpr int kDispatchWarps = EP_FP8_WARPS;  // warps per block
 constexpr int kRowRegs = 8;        // destination rows held in registers per pass
 
 // FP8: each lane owns 16 consecutive channels (two 16-byte loads, one
-// 16-byte store of codes per destination row); 8 lanes form one 128-channel
-// block; a warp covers 512 channels per group and EP_FP8_U groups per
-// iteration (their loads are issued together).
-struct Fp8Group {
-    uint4 q;   // 16 e4m3 codes of this lane
-    float sf;  // scale of this lane's 128-channel block
-};
-
-__device__ __forceinline__ Fp8Group quantize16(const uint4& a, const uint4& b) {
-    const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float f[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        f[2 * i] = bf16lo_to_f32(wv[i]);
-        f[2 * i + 1] = bf16hi_to_f32(wv[i]);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-    const float ap = fmaxf(amax, 1e-4f);
-    Fp8Group g;
-    g.sf = __fdiv_rn(ap, 448.0f);
-    const float inv = __fdiv_rn(448.0f, ap);
-    uint32_t qw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t lo =
-            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
-        const uint32_t hi =
-            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
-        qw[i] = lo | (hi << 16);
-    }
-    g.q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-    return g;
-}
-
+// 16-byte store of codes per destination row; quantize16 in ep_internal.cuh);
+// 8 lanes form one 128-channel block; a warp covers 512 channels per group
+// and EP_FP8_U groups per iteration (their loads are issued together).
 __global__ void EP_FP8_BOUNDS
 dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k, int S,
                     int64_t slice_ch, const int32_t* __restrict__ dst_row,

@@ -204,6 +204,46 @@ __device__ __forceinline__ int load_dst_row(const int32_t* __restrict__ dst_row,
     return r;
 }
 
+// ---- per-token FP8 e4m3 cast of one lane's 16 channels --------------------
+// 8 consecutive lanes hold one 128-channel block: its amax comes from three
+// xor-shuffles, the scale is max(amax, 1e-4) / 448 and the codes are
+// e4m3_rn_satfinite(x * (448 / max(amax, 1e-4))), both divisions IEEE.
+struct Fp8Group {
+    uint4 q;   // 16 e4m3 codes of this lane
+    float sf;  // scale of this lane's 128-channel block
+};
+
+__device__ __forceinline__ Fp8Group quantize16(const uint4& a, const uint4& b) {
+    const uint32_t wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16lo_to_f32(wv[i]);
+        f[2 * i + 1] = bf16hi_to_f32(wv[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+    const float ap = fmaxf(amax, 1e-4f);
+    Fp8Group g;
+    g.sf = __fdiv_rn(ap, 448.0f);
+    const float inv = __fdiv_rn(448.0f, ap);
+    uint32_t qw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo =
+            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
+        const uint32_t hi =
+            cvt_e4m3x2_rn_sat(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
+        qw[i] = lo | (hi << 16);
+    }
+    g.q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    return g;
+}
+
 // Row index of warp g when each row has S column slices.  S > 1 only when
 // the grid holds fewer than 2 * EP_SLICE_WARPS_PER_SM warps per SM, so g then
 // fits 32 bits and a 32-bit division suffices; S == 1 needs none.
@@ -373,6 +413,15 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
                           int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
                           int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
                           int32_t* workspace, cudaStream_t stream);
+
+// Layout and dispatch in one launch for few tokens; cudaErrorNotSupported
+// (nothing enqueued) when the shape is outside the fused kernel's range.
+cudaError_t launch_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                                   int kind, int capacity, const void* x, int64_t H, bool fp8,
+                                   int32_t* expert_counts, int32_t* expert_offsets,
+                                   int32_t* dst_row, int32_t* rank_token_counts, void* recv,
+                                   float* recv_scale, int64_t rows, uint32_t* status,
+                                   cudaStream_t stream);
 
 cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
                                  const int32_t* dst_row, void* recv, int64_t rows,

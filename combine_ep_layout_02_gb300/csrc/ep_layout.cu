@@ -743,6 +743,217 @@ cudaError_t try_cluster(int nt, const int32_t* topk_idx, int64_t T, int k, int E
     return cudaErrorNotSupported;
 }
 
+// ---- layout fused with dispatch (few tokens) --------------------------------
+// One launch for ep_layout_dispatch: every block computes the whole layout in
+// shared memory with the single-block algorithm above, then each of its warps
+// dispatches one (token, column slice) unit from it.  Block 0 alone stores the
+// layout outputs and the status word; every block derives the same flags
+// (bad ids, masked overflow, rows outside the dispatch buffer), so no block
+// races another on the status.  Each warp loads its slice of x before the
+// layout, so those loads overlap the layout's latency.
+constexpr int kLDThreads = 256;
+constexpr int kLDWarps = kLDThreads / 32;
+constexpr int kLDMaxTokens = 128;  // above, the two launches measured faster (256 tokens: 8.8 vs 11.3 us)
+
+// warp_assign_pairs for the fused kernel: slots into s_out (and g_out if
+// given), conditions OR-ed into the block's flag word.
+__device__ __forceinline__ void warp_assign_pairs_shared(const int32_t* s_ids, int wpairs, int E,
+                                                         int kind, int capacity, int32_t* my_w,
+                                                         const int32_t* s_off, int32_t* s_out,
+                                                         int32_t* __restrict__ g_out, int64_t rows,
+                                                         uint32_t* s_flags) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = lanemask_lt();
+    const int key_bits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);
+    for (int q0 = 0; q0 < wpairs; q0 += 32) {  // warp-uniform
+        const int q = q0 + lane;
+        const bool in_range = q < wpairs;
+        const int e = in_range ? s_ids[q] : -1;
+        const bool valid = (e >= 0) && (e < E);
+        const bool bad = in_range && !valid && e != -1;
+        const unsigned peers = warp_peers(valid, e, key_bits);
+        bool overflow = false;
+        int dst = -1;
+        if (valid) {
+            const int slot = my_w[e] + __popc(peers & lt);
+            if (kind == EP_LAYOUT_CONTIGUOUS) {
+                dst = s_off[e] + slot;
+            } else if (slot < capacity) {
+                dst = e * capacity + slot;
+            } else {
+                overflow = true;
+            }
+        }
+        if (in_range) {
+            s_out[q] = dst;
+            if (g_out) g_out[q] = dst;
+        }
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) my_w[e] += __popc(peers);
+        __syncwarp();
+        const unsigned f = (__ballot_sync(kFullMask, bad) ? EP_FLAG_BAD_EXPERT : 0u) |
+                           (__ballot_sync(kFullMask, overflow) ? EP_FLAG_OVERFLOW : 0u) |
+                           (__ballot_sync(kFullMask, (int64_t)dst >= rows) ? EP_FLAG_BAD_ROW : 0u);
+        if (f && lane == 0) atomicOr(s_flags, f);
+    }
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kLDThreads)
+layout_dispatch_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
+                       int capacity, int tpw, const uint16_t* __restrict__ x, int64_t H, int S,
+                       int64_t slice, int32_t* __restrict__ expert_counts,
+                       int32_t* __restrict__ expert_offsets, int32_t* __restrict__ dst_row,
+                       int32_t* __restrict__ rank_token_counts, void* __restrict__ recv,
+                       float* __restrict__ recv_scale, int64_t rows, uint32_t* __restrict__ status) {
+    constexpr int NT = kLDThreads;
+    constexpr int NW = kLDWarps;
+    constexpr int U = FP8 ? 2 : 4;  // 512-channel groups (FP8) or 16-byte vectors per pass
+    extern __shared__ __align__(16) int32_t smem_i[];
+    __shared__ uint32_t s_flags;
+    const int ES = E | 1;
+    const int npairs = T * k;
+    const int npad = NW * tpw * k;              // >= npairs
+    int32_t* s_idx = smem_i;                    // [npad]
+    int32_t* s_dst = s_idx + npad;              // [npad]
+    int32_t* s_w = s_dst + npad;                // [NW][ES]
+    int32_t* s_tot = s_w + NW * ES;             // [E]
+    int32_t* s_off = s_tot + E;                 // [E + 1]
+    int32_t* s_rank = s_off + E + 1;            // [R_cols]
+    int32_t* s_rank_of = s_rank + R_cols;       // [E]
+    int32_t* s_warp = s_rank_of + E;            // [NW]
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const bool lead = blockIdx.x == 0;
+
+    pdl_wait();
+    pdl_trigger();
+
+    // this warp's unit: token t, columns [cb, ce) in units of 8 channels
+    // (BF16 vectors) or 16 channels (FP8 lane groups)
+    const int64_t unit = (int64_t)blockIdx.x * NW + warp;
+    const int64_t t = slice_row(unit, S);
+    const bool has_unit = t < T;  // warp-uniform
+    const int64_t nunits = FP8 ? H / 16 : H / 8;
+    const int64_t cb = has_unit ? (unit - t * S) * slice : 0;
+    const int64_t ce = has_unit ? (cb + slice < nunits ? cb + slice : nunits) : 0;
+    const uint16_t* src = x + (has_unit ? t : 0) * H;
+    uint4 pa[U], pb[U];  // the first pass of this unit, loaded before the layout
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t c = cb + u * 32 + lane;  // unit index
+        pa[u] = make_uint4(0, 0, 0, 0);
+        pb[u] = make_uint4(0, 0, 0, 0);
+        if (c < ce) {
+            if (FP8) {
+                pa[u] = ld_stream_v4(src + c * 16);
+                pb[u] = ld_stream_v4(src + c * 16 + 8);
+            } else {
+                pa[u] = ld_stream_v4(src + c * 8);
+            }
+        }
+    }
+
+    // ---- the layout, as layout_fused_kernel, into shared memory
+    if (threadIdx.x == 0) s_flags = 0u;
+    stage_ids(idx, 0, npairs, npad, s_idx);
+    for (int i = threadIdx.x; i < NW * ES; i += NT) s_w[i] = 0;
+    for (int i = threadIdx.x; i < R_cols; i += NT) s_rank[i] = 0;
+    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
+    __syncthreads();
+    const int wp0 = warp * tpw * k;
+    const int wrem = npairs - wp0;
+    const int wpairs = wrem <= 0 ? 0 : (wrem < tpw * k ? wrem : tpw * k);
+    int32_t* my_w = s_w + warp * ES;
+    warp_count_pairs(s_idx + wp0, wpairs, E, my_w);
+    if (R_cols > 0)
+        for (int tt = threadIdx.x; tt < T; tt += NT)
+            count_token_ranks(s_idx + tt * k, k, E, R_cols, s_rank_of, s_rank);
+    __syncthreads();
+    warp_hist_prefix<NT>(s_w, ES, E, s_tot);
+    __syncthreads();
+    if (lead)
+        for (int e = threadIdx.x; e < E; e += NT) expert_counts[e] = s_tot[e];
+    block_exclusive_scan<NT>(s_tot, E, s_off, s_warp);
+    if (lead) {
+        for (int e = threadIdx.x; e <= E; e += NT) expert_offsets[e] = s_off[e];
+        for (int r = threadIdx.x; r < R_cols; r += NT) rank_token_counts[r] = s_rank[r];
+    }
+    warp_assign_pairs_shared(s_idx + wp0, wpairs, E, kind, capacity, my_w, s_off, s_dst + wp0,
+                             lead ? dst_row + wp0 : nullptr, rows, &s_flags);
+    __syncthreads();  // s_dst and s_flags complete
+    if (lead && threadIdx.x == 0 && status) *status = s_flags;
+    if (!has_unit) return;
+
+    // ---- dispatch of this warp's unit from the shared layout
+    int my_row = -1;
+    if (lane < k) {
+        const int d = s_dst[t * k + lane];
+        my_row = (d >= 0 && (int64_t)d < rows) ? d : -1;  // out-of-range rows were flagged
+    }
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        int rr[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
+            rr[jj] = (j0 + jj < k) ? r : -1;
+        }
+        for (int64_t c0 = cb; c0 < ce; c0 += 32 * U) {
+            uint4 a[U], b[U];
+            if (j0 == 0 && c0 == cb) {  // warp-uniform: the loads issued before the layout
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    a[u] = pa[u];
+                    b[u] = pb[u];
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t c = c0 + u * 32 + lane;
+                    a[u] = make_uint4(0, 0, 0, 0);
+                    b[u] = make_uint4(0, 0, 0, 0);
+                    if (c < ce) {
+                        if (FP8) {
+                            a[u] = ld_stream_v4(src + c * 16);
+                            b[u] = ld_stream_v4(src + c * 16 + 8);
+                        } else {
+                            a[u] = ld_stream_v4(src + c * 8);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + u * 32 + lane;
+                const bool act = c < ce;  // FP8: all 8 lanes of a 128-channel block agree
+                if (FP8) {
+                    const Fp8Group g = quantize16(a[u], b[u]);
+                    uint8_t* q = static_cast<uint8_t*>(recv);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        if (rr[jj] < 0) continue;  // warp-uniform
+                        if (act) st_v4(q + (int64_t)rr[jj] * H + c * 16, g.q);
+                        if (act && (lane & 7) == 0)
+                            recv_scale[(int64_t)rr[jj] * (H / 128) + (c >> 3)] = g.sf;
+                    }
+                } else {
+                    uint4* v = static_cast<uint4*>(recv);
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        if (rr[jj] < 0) continue;  // warp-uniform
+                        if (act) st_cs_v4(v + (int64_t)rr[jj] * (H / 8) + c, a[u]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+size_t layout_dispatch_smem_bytes(int tpw, int k, int E, int R_cols) {
+    return ((size_t)2 * kLDWarps * tpw * k + (size_t)kLDWarps * (E | 1) + 3 * (size_t)E + 1 +
+            R_cols + kLDWarps) * sizeof(int32_t);
+}
+
 }  // namespace
 
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
@@ -779,6 +990,30 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
     return launch_pdl(layout_assign_kernel, dim3((unsigned)nchunk), dim3(kLayoutThreads),
                       assign_smem_bytes(k, E), stream, topk_idx, T, k, E, kind, capacity, align, nchunk,
                       workspace, expert_counts, expert_offsets, dst_row, status);
+}
+
+cudaError_t launch_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                                   int kind, int capacity, const void* x, int64_t H, bool fp8,
+                                   int32_t* expert_counts, int32_t* expert_offsets,
+                                   int32_t* dst_row, int32_t* rank_token_counts, void* recv,
+                                   float* recv_scale, int64_t rows, uint32_t* status,
+                                   cudaStream_t stream) {
+    if (T < 1 || T > kLDMaxTokens) return cudaErrorNotSupported;
+    const int R_cols = rank_token_counts ? R : 0;
+    const int tpw = (int)((T + kLDWarps - 1) / kLDWarps);
+    const size_t smem = layout_dispatch_smem_bytes(tpw, k, E, R_cols);
+    if (smem > kFusedSmemLimit) return cudaErrorNotSupported;
+    const RowSlices sl = row_slices(T, fp8 ? H / 16 : H / 8);
+    const unsigned grid = (unsigned)((T * sl.S + kLDWarps - 1) / kLDWarps);
+    static std::atomic<uint64_t> configured_bf16{0}, configured_fp8{0};
+    cudaError_t err = fp8 ? raise_smem_limit(layout_dispatch_kernel<true>, configured_fp8)
+                          : raise_smem_limit(layout_dispatch_kernel<false>, configured_bf16);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(fp8 ? layout_dispatch_kernel<true> : layout_dispatch_kernel<false>,
+                      dim3(grid), dim3(kLDThreads), smem, stream, topk_idx, (int)T, k, E, R_cols,
+                      kind, capacity, tpw, static_cast<const uint16_t*>(x), H, sl.S, sl.slice,
+                      expert_counts, expert_offsets, dst_row, rank_token_counts, recv, recv_scale,
+                      rows, status);
 }
 
 }  // namespace ep

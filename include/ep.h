@@ -224,6 +224,34 @@ EP_API int ep_dispatch_fp8(const void* x, int64_t T, int64_t H, int k, const int
                     uint32_t* status, void* stream);
 
 /*
+ * ep_layout_dispatch -- ep_layout followed by ep_dispatch on the same status
+ * word, in one call (PR #1238, "What changed": the dispatch layout is part
+ * of the timed dispatch boundary, and the Decode-like profile measures 128
+ * tokens per rank, where separate launches dominate).  Arguments are those
+ * of the two calls; the layout kind, capacity and rank counts are as for
+ * ep_layout (no alignment), recv and rows as for ep_dispatch.  The outputs
+ * (counts, offsets, dst_row, rank_token_counts, recv, status) are identical
+ * to the two calls made in sequence.  Up to 128 tokens this is one kernel
+ * launch: every block computes the whole layout in shared memory and
+ * dispatches its share of the rows; larger batches run the two launches.
+ * The workspace rules of ep_layout apply.
+ */
+EP_API int ep_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
+                              int capacity, const void* x, int64_t H, int32_t* expert_counts,
+                              int32_t* expert_offsets, int32_t* dst_row,
+                              int32_t* rank_token_counts, void* recv, int64_t rows,
+                              uint32_t* status, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* ep_layout_dispatch_fp8 -- the same with ep_dispatch_fp8 (H % 128 == 0). */
+EP_API int ep_layout_dispatch_fp8(const int32_t* topk_idx, int64_t T, int k, int E, int R,
+                                  int kind, int capacity, const void* x, int64_t H,
+                                  int32_t* expert_counts, int32_t* expert_offsets,
+                                  int32_t* dst_row, int32_t* rank_token_counts, uint8_t* recv_q,
+                                  float* recv_scale, int64_t rows, uint32_t* status,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * ep_combine -- weighted top-k reduction back into token order (the combine
  * step of the PR's timed boundary; BF16 in either payload mode):
  *     out[t, h] = bf16_rne( sum over j with dst_row[t,j] != -1 of

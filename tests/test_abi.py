@@ -91,6 +91,25 @@ def test_layout_argument_validation(lib):
     assert call(ws=ctypes.c_void_p((1 << 20) + 4)) == 2
 
 
+def test_layout_dispatch_argument_validation(lib):
+    def call(fp8=False, T=16, k=8, E=256, R=16, kind=0, cap=0, H=64, x=FAKE, idx=FAKE, ws=FAKE,
+             wsb=1 << 30, recv=FAKE, rows=128):
+        if fp8:
+            return lib.ep_layout_dispatch_fp8(idx, T, k, E, R, kind, cap, x, H, FAKE, FAKE, FAKE,
+                                              None, recv, FAKE, rows, None, ws, wsb, None)
+        return lib.ep_layout_dispatch(idx, T, k, E, R, kind, cap, x, H, FAKE, FAKE, FAKE, None,
+                                      recv, rows, None, ws, wsb, None)
+    assert call(E=255) == 1                    # the layout's checks: E % R != 0
+    assert call(k=33) == 1
+    assert call(ws=None) == 3
+    assert call(H=100) == 2                    # the dispatch's: H % 8
+    assert call(fp8=True, H=64) == 2           # FP8: H % 128
+    assert call(x=None) == 1
+    assert call(recv=None) == 1
+    assert call(x=ctypes.c_void_p((1 << 20) + 8)) == 2
+    assert call(fp8=True, H=128, recv=ctypes.c_void_p((1 << 20) + 4)) == 2
+
+
 def test_dispatch_combine_argument_validation(lib):
     assert lib.ep_dispatch(FAKE, 4, 100, 8, FAKE, FAKE, 32, None, None) == 2        # H % 8
     assert lib.ep_dispatch(FAKE, 4, 64, 0, FAKE, FAKE, 32, None, None) == 1          # k

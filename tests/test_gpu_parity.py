@@ -499,3 +499,62 @@ def test_dispatch_fp8_every_pattern_at_fixed_scales():
     rq, rs = oracle.dispatch_fp8(allv, dst.cpu().numpy(), T)
     assert np.array_equal(q.cpu().numpy(), rq)
     assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+# --------------------------------------------------------------------------- layout + dispatch in one call
+
+@pytest.mark.parametrize("T,k,E,R,kind,cap,H,fp8,rows_cut,bad", [
+    (128, 8, 128, 4, "contiguous", 0, 2048, False, 0, False),      # the small workload's shape
+    (1, 8, 64, 4, "contiguous", 0, 7168, False, 0, False),
+    (1, 8, 64, 4, "contiguous", 0, 7168, True, 0, False),
+    (37, 13, 32, 4, "contiguous", 0, 1336, False, 0, False),       # k > 8, ragged slices
+    (200, 8, 64, 8, "masked", 10, 256, False, 0, False),           # capacity overflow
+    (128, 8, 256, 16, "contiguous", 0, 7168, True, 0, False),      # largest fused batch
+    (120, 8, 256, 16, "masked", 128, 1024, False, 0, True),        # bad expert ids
+    (256, 8, 256, 16, "masked", 256, 1024, False, 0, True),        # bad ids, two launches
+    (100, 8, 64, 4, "contiguous", 0, 512, False, 7, False),        # rows too few: BAD_ROW
+    (257, 8, 256, 16, "contiguous", 0, 1024, True, 0, False),      # above the fused range
+    (3000, 8, 256, 16, "masked", 3000, 512, False, 0, False),
+])
+def test_layout_dispatch_matches_oracle(T, k, E, R, kind, cap, H, fp8, rows_cut, bad):
+    rng = np.random.default_rng(T * 31 + H + k)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    if bad:
+        idx[3, 2] = E + 3
+        idx[5, 0] = -7
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32) * 2).to(torch.bfloat16)
+    okind = oracle.LAYOUT_MASKED if kind == "masked" else oracle.LAYOUT_CONTIGUOUS
+    ref = oracle.layout(idx, E, R, okind, cap)
+    rows = (T * k if kind == "contiguous" else E * cap) - rows_cut
+    xd, idd = x.to(DEV), torch.from_numpy(idx).to(DEV)
+    if fp8:
+        q0 = torch.full((rows, H), 0x5A, dtype=torch.uint8, device=DEV)
+        s0 = torch.full((rows, H // 128), -1.0, dtype=torch.float32, device=DEV)
+        lay, q, sc = ep.layout_dispatch(xd, idd, E, R, kind, cap, rows, fp8=True, recv_q=q0,
+                                        recv_scale=s0)
+    else:
+        r0 = torch.full((rows, H), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        lay, recv = ep.layout_dispatch(xd, idd, E, R, kind, cap, rows, recv=r0)
+    assert np.array_equal(lay.expert_counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(lay.expert_offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(lay.dst_row.cpu().numpy(), ref["dst_row"])
+    assert np.array_equal(lay.rank_token_counts.cpu().numpy(), ref["rank_token_counts"])
+    expect_flags = ref["flags"] | (ep.EP_FLAG_BAD_ROW if (ref["dst_row"] >= rows).any() else 0)
+    assert ep.status_read(lay.status) == expect_flags
+    dst = np.where(ref["dst_row"] < rows, ref["dst_row"], -1)       # rows past the buffer are skipped
+    if fp8:
+        rq, rs = oracle.dispatch_fp8(_bits(x), dst, rows, recv_q=np.full((rows, H), 0x5A, np.uint8),
+                                     recv_scale=np.full((rows, H // 128), -1.0, np.float32))
+        assert np.array_equal(q.cpu().numpy(), rq)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    else:
+        rr = oracle.dispatch_bf16(_bits(x), dst, rows, recv=np.full((rows, H), np.uint16(0xABCD), np.uint16))
+        assert np.array_equal(_bits(recv), rr)
+
+
+def test_layout_dispatch_empty_batch():
+    idx = torch.zeros(0, 8, dtype=torch.int32, device=DEV)
+    x = torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV)
+    lay, recv = ep.layout_dispatch(x, idx, 64, 4)
+    assert int(lay.expert_counts.abs().sum()) == 0 and int(lay.expert_offsets.abs().sum()) == 0
+    assert ep.status_read(lay.status) == 0 and recv.shape == (0, 256)
