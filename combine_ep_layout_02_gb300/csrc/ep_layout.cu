@@ -445,6 +445,63 @@ __device__ __forceinline__ void warp_assign_pairs(const int32_t* s_ids, int wpai
     }
 }
 
+// Shared-memory arrays of the single-block layout (carved by the caller).
+struct BlockLayoutSmem {
+    int32_t* idx;      // [npad] staged ids (npad = warps * tpw * k >= T * k)
+    int32_t* w;        // [warps][E | 1] per-warp histograms, then base slots
+    int32_t* tot;      // [E] (padded) segment lengths
+    int32_t* off;      // [E + 1] their exclusive scan
+    int32_t* rank;     // [R_cols] tokens per virtual rank
+    int32_t* rank_of;  // [E]
+    int32_t* warp;     // [warps] scan scratch
+};
+
+// The single-block layout up to the slot walk, for T tokens in one block of
+// NT threads (warp w owns tokens [w*tpw, (w+1)*tpw)): ids staged, per-warp
+// histograms and their exclusive prefix over the warps, expert totals
+// (stored to expert_counts when given), segment lengths rounded up to
+// `align` and scanned into sm.off (stored to expert_offsets when given), and
+// the tokens per rank (stored to rank_token_counts when given).  Ends with
+// the block synchronised.
+template <int NT>
+__device__ void block_layout_scan(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols,
+                                  int align, int tpw, const BlockLayoutSmem& sm,
+                                  int32_t* __restrict__ expert_counts,
+                                  int32_t* __restrict__ expert_offsets,
+                                  int32_t* __restrict__ rank_token_counts) {
+    constexpr int NW = NT / 32;
+    const int ES = E | 1;
+    const int npairs = T * k;
+    const int npad = NW * tpw * k;
+    const int warp = threadIdx.x >> 5;
+    stage_ids(idx, 0, npairs, npad, sm.idx);
+    for (int i = threadIdx.x; i < NW * ES; i += NT) sm.w[i] = 0;
+    for (int i = threadIdx.x; i < R_cols; i += NT) sm.rank[i] = 0;
+    if (R_cols > 0) fill_rank_table(E, R_cols, sm.rank_of);
+    __syncthreads();
+    const int wp0 = warp * tpw * k;
+    const int wrem = npairs - wp0;
+    const int wpairs = wrem <= 0 ? 0 : (wrem < tpw * k ? wrem : tpw * k);
+    warp_count_pairs(sm.idx + wp0, wpairs, E, sm.w + warp * ES);
+    if (R_cols > 0)
+        for (int t = threadIdx.x; t < T; t += NT)
+            count_token_ranks(sm.idx + t * k, k, E, R_cols, sm.rank_of, sm.rank);
+    __syncthreads();
+    warp_hist_prefix<NT>(sm.w, ES, E, sm.tot);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += NT) {
+        const int c = sm.tot[e];
+        if (expert_counts) expert_counts[e] = c;
+        if (align > 1) sm.tot[e] = (c + align - 1) / align * align;  // padded segment length
+    }
+    __syncthreads();
+    block_exclusive_scan<NT>(sm.tot, E, sm.off, sm.warp);
+    if (expert_offsets)
+        for (int e = threadIdx.x; e <= E; e += NT) expert_offsets[e] = sm.off[e];
+    if (rank_token_counts)
+        for (int r = threadIdx.x; r < R_cols; r += NT) rank_token_counts[r] = sm.rank[r];
+}
+
 // Small batches (T <= kFusedMaxTokens): the whole layout in one block of NT
 // threads; warp w owns tokens [w*tpw, (w+1)*tpw).  The block scan over the
 // expert totals gives the offsets -- the same stable slots as the chunked
@@ -461,47 +518,26 @@ layout_fused_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     const int ES = E | 1;
     const int npairs = T * k;
     const int npad = NW * tpw * k;              // >= npairs
-    int32_t* s_idx = smem_i;                    // [npad]
-    int32_t* s_w = s_idx + npad;                // [NW][ES]
-    int32_t* s_tot = s_w + NW * ES;             // [E]
-    int32_t* s_off = s_tot + E;                 // [E + 1]
-    int32_t* s_rank = s_off + E + 1;            // [R_cols]
-    int32_t* s_rank_of = s_rank + R_cols;       // [E]
-    int32_t* s_warp = s_rank_of + E;            // [NW]
+    BlockLayoutSmem sm;
+    sm.idx = smem_i;                            // [npad]
+    sm.w = sm.idx + npad;                       // [NW][ES]
+    sm.tot = sm.w + NW * ES;                    // [E]
+    sm.off = sm.tot + E;                        // [E + 1]
+    sm.rank = sm.off + E + 1;                   // [R_cols]
+    sm.rank_of = sm.rank + R_cols;              // [E]
+    sm.warp = sm.rank_of + E;                   // [NW]
     const int warp = threadIdx.x >> 5;
 
     pdl_wait();
     pdl_trigger();
     if (threadIdx.x == 0 && status) *status = 0u;
-    stage_ids(idx, 0, npairs, npad, s_idx);
-    for (int i = threadIdx.x; i < NW * ES; i += NT) s_w[i] = 0;
-    for (int i = threadIdx.x; i < R_cols; i += NT) s_rank[i] = 0;
-    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
-    __syncthreads();
-
+    block_layout_scan<NT>(idx, T, k, E, R_cols, align, tpw, sm, expert_counts, expert_offsets,
+                          rank_token_counts);
     const int wp0 = warp * tpw * k;
     const int wrem = npairs - wp0;
     const int wpairs = wrem <= 0 ? 0 : (wrem < tpw * k ? wrem : tpw * k);
-    int32_t* my_w = s_w + warp * ES;
-    warp_count_pairs(s_idx + wp0, wpairs, E, my_w);
-    if (R_cols > 0)
-        for (int t = threadIdx.x; t < T; t += NT)
-            count_token_ranks(s_idx + t * k, k, E, R_cols, s_rank_of, s_rank);
-    __syncthreads();
-    warp_hist_prefix<NT>(s_w, ES, E, s_tot);
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += NT) {
-        const int c = s_tot[e];
-        expert_counts[e] = c;
-        if (align > 1) s_tot[e] = (c + align - 1) / align * align;  // padded segment length
-    }
-    __syncthreads();
-    block_exclusive_scan<NT>(s_tot, E, s_off, s_warp);
-    for (int e = threadIdx.x; e <= E; e += NT) expert_offsets[e] = s_off[e];
-    for (int r = threadIdx.x; r < R_cols; r += NT) rank_token_counts[r] = s_rank[r];
-
-    warp_assign_pairs(s_idx + wp0, wpairs, E, kind, capacity, my_w, nullptr, s_off, dst_row + wp0,
-                      status);
+    warp_assign_pairs(sm.idx + wp0, wpairs, E, kind, capacity, sm.w + warp * ES, nullptr, sm.off,
+                      dst_row + wp0, status);
 }
 
 // Medium batches (T <= kClusterMaxTokens): the whole layout in ONE launch of
@@ -814,14 +850,15 @@ layout_dispatch_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int
     const int ES = E | 1;
     const int npairs = T * k;
     const int npad = NW * tpw * k;              // >= npairs
-    int32_t* s_idx = smem_i;                    // [npad]
-    int32_t* s_dst = s_idx + npad;              // [npad]
-    int32_t* s_w = s_dst + npad;                // [NW][ES]
-    int32_t* s_tot = s_w + NW * ES;             // [E]
-    int32_t* s_off = s_tot + E;                 // [E + 1]
-    int32_t* s_rank = s_off + E + 1;            // [R_cols]
-    int32_t* s_rank_of = s_rank + R_cols;       // [E]
-    int32_t* s_warp = s_rank_of + E;            // [NW]
+    int32_t* s_dst = smem_i;                    // [npad] slots of all pairs
+    BlockLayoutSmem sm;
+    sm.idx = s_dst + npad;                      // [npad]
+    sm.w = sm.idx + npad;                       // [NW][ES]
+    sm.tot = sm.w + NW * ES;                    // [E]
+    sm.off = sm.tot + E;                        // [E + 1]
+    sm.rank = sm.off + E + 1;                   // [R_cols]
+    sm.rank_of = sm.rank + R_cols;              // [E]
+    sm.warp = sm.rank_of + E;                   // [NW]
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const bool lead = blockIdx.x == 0;
@@ -856,31 +893,13 @@ layout_dispatch_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int
 
     // ---- the layout, as layout_fused_kernel, into shared memory
     if (threadIdx.x == 0) s_flags = 0u;
-    stage_ids(idx, 0, npairs, npad, s_idx);
-    for (int i = threadIdx.x; i < NW * ES; i += NT) s_w[i] = 0;
-    for (int i = threadIdx.x; i < R_cols; i += NT) s_rank[i] = 0;
-    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
-    __syncthreads();
+    block_layout_scan<NT>(idx, T, k, E, R_cols, 1, tpw, sm, lead ? expert_counts : nullptr,
+                          lead ? expert_offsets : nullptr, lead ? rank_token_counts : nullptr);
     const int wp0 = warp * tpw * k;
     const int wrem = npairs - wp0;
     const int wpairs = wrem <= 0 ? 0 : (wrem < tpw * k ? wrem : tpw * k);
-    int32_t* my_w = s_w + warp * ES;
-    warp_count_pairs(s_idx + wp0, wpairs, E, my_w);
-    if (R_cols > 0)
-        for (int tt = threadIdx.x; tt < T; tt += NT)
-            count_token_ranks(s_idx + tt * k, k, E, R_cols, s_rank_of, s_rank);
-    __syncthreads();
-    warp_hist_prefix<NT>(s_w, ES, E, s_tot);
-    __syncthreads();
-    if (lead)
-        for (int e = threadIdx.x; e < E; e += NT) expert_counts[e] = s_tot[e];
-    block_exclusive_scan<NT>(s_tot, E, s_off, s_warp);
-    if (lead) {
-        for (int e = threadIdx.x; e <= E; e += NT) expert_offsets[e] = s_off[e];
-        for (int r = threadIdx.x; r < R_cols; r += NT) rank_token_counts[r] = s_rank[r];
-    }
-    warp_assign_pairs_shared(s_idx + wp0, wpairs, E, kind, capacity, my_w, s_off, s_dst + wp0,
-                             lead ? dst_row + wp0 : nullptr, rows, &s_flags);
+    warp_assign_pairs_shared(sm.idx + wp0, wpairs, E, kind, capacity, sm.w + warp * ES, sm.off,
+                             s_dst + wp0, lead ? dst_row + wp0 : nullptr, rows, &s_flags);
     __syncthreads();  // s_dst and s_flags complete
     if (lead && threadIdx.x == 0 && status) *status = s_flags;
     if (!has_unit) return;
