@@ -2,8 +2,6 @@
 // Every check that can fail happens before anything is enqueued.
 #include <stdint.h>
 
-#include <atomic>
-
 #include "ep_internal.cuh"
 
 namespace {
@@ -34,17 +32,19 @@ int check_rows_args(int64_t T, int64_t H, int k, int64_t rows) {
 namespace ep {
 void record_cuda_error(int err) { g_last_cuda_error = err; }
 
+int cached_device_attribute(cudaDeviceAttr attr, std::atomic<int> (&cache)[64]) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    v = cache[dev & 63].load(std::memory_order_relaxed);
+    if (v == 0 && cudaDeviceGetAttribute(&v, attr, dev) == cudaSuccess && v > 0)
+        cache[dev & 63].store(v, std::memory_order_relaxed);
+    return v > 0 ? v : 0;
+}
+
 RowSlices row_slices(int64_t T, int64_t nvec) {
     // SM count per device, read once (it only shapes grids)
     static std::atomic<int> sm_cache[64];
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) {
-        sms = sm_cache[dev & 63].load(std::memory_order_relaxed);
-        if (sms == 0 &&
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-            sms > 0)
-            sm_cache[dev & 63].store(sms, std::memory_order_relaxed);
-    }
+    int sms = cached_device_attribute(cudaDevAttrMultiProcessorCount, sm_cache);
     if (sms <= 0) sms = 1;
     const int64_t target = (int64_t)sms * EP_SLICE_WARPS_PER_SM;
     int64_t S = 1;

@@ -7,8 +7,6 @@
 // rows, so every input byte is read once and every output byte written once:
 // the HBM floor is T*H*2 read + T*k*H*2 written.  Large batches run at most
 // one 8-warp block per SM, where this write-bound scatter is fastest.
-#include <atomic>
-
 #include "ep_internal.cuh"
 
 #ifndef EP_DISPATCH_BULK
@@ -168,40 +166,15 @@ dispatch_bf16_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, uint32_t row
 }
 
 // Dynamic shared memory that admits one block per SM: just over half of an
-// SM's shared memory (0 if the device reports none).  Per device, read once.
+// SM's shared memory (0, no request, if the device reports too little).
 size_t dispatch_occupancy_smem() {
-    static std::atomic<int> cache[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    int v = cache[dev & 63].load(std::memory_order_relaxed);
-    if (v == 0) {
-        int per_sm = 0, per_block = 0;
-        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
-                cudaSuccess ||
-            cudaDeviceGetAttribute(&per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-                cudaSuccess)
-            return 0;
-        v = per_sm / 2 + 1024;
-        if (v > per_block) v = -1;  // cannot be enforced this way: no request
-        cache[dev & 63].store(v, std::memory_order_relaxed);
-    }
-    return v > 0 ? (size_t)v : 0;
-}
-
-// Raise `kernel`'s dynamic shared-memory limit to `bytes`, once per device.
-template <typename K>
-cudaError_t raise_smem_limit_once(K kernel, size_t bytes) {
-    static std::atomic<uint64_t> configured{0};
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-        if (err != cudaSuccess) return err;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
-    }
-    return cudaSuccess;
+    static std::atomic<int> per_sm_cache[64], per_block_cache[64];
+    const int per_sm =
+        cached_device_attribute(cudaDevAttrMaxSharedMemoryPerMultiprocessor, per_sm_cache);
+    const int per_block =
+        cached_device_attribute(cudaDevAttrMaxSharedMemoryPerBlockOptin, per_block_cache);
+    const int v = per_sm / 2 + 1024;
+    return (per_sm > 0 && v <= per_block) ? (size_t)v : 0;
 }
 
 }  // namespace
@@ -249,7 +222,8 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
     auto kern = dispatch_bf16_kernel<EP_DISPATCH_U, true>;
     const size_t smem = dispatch_occupancy_smem();
     if (smem > 0) {
-        const cudaError_t e = raise_smem_limit_once(kern, smem);
+        static std::atomic<uint64_t> configured{0};
+        const cudaError_t e = raise_smem_limit(kern, smem, configured);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(kern, dim3(grid), dim3(kDispatchWarps * 32), smem, stream,

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "ep.h"
@@ -364,6 +365,26 @@ __device__ __forceinline__ void reduce_rows(const uint4* __restrict__ rows, int6
 
 // Record a CUDA error for ep_last_cuda_error() (host, per thread).
 void record_cuda_error(int err);
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes`, once per device;
+// `configured` is that kernel's flag word (one bit per device ordinal).
+template <typename K>
+cudaError_t raise_smem_limit(K kernel, size_t bytes, std::atomic<uint64_t>& configured) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (err != cudaSuccess) return err;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    return cudaSuccess;
+}
+
+// An attribute of the current device, read once per device into the
+// caller's `cache` (0 = not read yet); 0 if it cannot be read.
+int cached_device_attribute(cudaDeviceAttr attr, std::atomic<int> (&cache)[64]);
 
 // Launch `kernel` with programmatic stream serialisation allowed, so that its
 // launch overlaps the tail of the previous kernel in the stream.  Every kernel

@@ -32,8 +32,6 @@
 // a multiple of m rows: the offsets scan ceil(count / m) * m instead.
 #include <cooperative_groups.h>
 
-#include <atomic>
-
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -665,30 +663,13 @@ size_t fused_smem_bytes(int warps, int tpw, int k, int E, int R_cols) {
 
 constexpr size_t kFusedSmemLimit = 160 * 1024;
 
-// Raise a kernel's dynamic shared-memory limit to kFusedSmemLimit, once per
-// device and kernel (the flag word is the caller's, one per kernel).
-template <typename K>
-cudaError_t raise_smem_limit(K kernel, std::atomic<uint64_t>& configured) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kFusedSmemLimit);
-        if (err != cudaSuccess) return err;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
-    }
-    return cudaSuccess;
-}
-
 template <int NT>
 cudaError_t launch_fused(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols, int kind,
                          int capacity, int align, int tpw, int32_t* expert_counts,
                          int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
                          uint32_t* status, size_t smem, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};
-    cudaError_t err = raise_smem_limit(layout_fused_kernel<NT>, configured);
+    cudaError_t err = raise_smem_limit(layout_fused_kernel<NT>, kFusedSmemLimit, configured);
     if (err != cudaSuccess) return err;
     return launch_pdl(layout_fused_kernel<NT>, dim3(1), dim3(NT), smem, stream, topk_idx, (int)T,
                       k, E, R_cols, kind, capacity, align, tpw, expert_counts, expert_offsets,
@@ -735,7 +716,7 @@ cudaError_t launch_cluster(const int32_t* topk_idx, int64_t T, int k, int E, int
                            int32_t* expert_offsets, int32_t* dst_row, int32_t* rank_token_counts,
                            uint32_t* status, size_t smem, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};
-    cudaError_t err = raise_smem_limit(layout_cluster_kernel<NT>, configured);
+    cudaError_t err = raise_smem_limit(layout_cluster_kernel<NT>, kFusedSmemLimit, configured);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kClusterBlocks);
@@ -1027,8 +1008,9 @@ cudaError_t launch_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, in
     const RowSlices sl = row_slices(T, fp8 ? H / 16 : H / 8);
     const unsigned grid = (unsigned)((T * sl.S + kLDWarps - 1) / kLDWarps);
     static std::atomic<uint64_t> configured_bf16{0}, configured_fp8{0};
-    cudaError_t err = fp8 ? raise_smem_limit(layout_dispatch_kernel<true>, configured_fp8)
-                          : raise_smem_limit(layout_dispatch_kernel<false>, configured_bf16);
+    cudaError_t err =
+        fp8 ? raise_smem_limit(layout_dispatch_kernel<true>, kFusedSmemLimit, configured_fp8)
+            : raise_smem_limit(layout_dispatch_kernel<false>, kFusedSmemLimit, configured_bf16);
     if (err != cudaSuccess) return err;
     return launch_pdl(fp8 ? layout_dispatch_kernel<true> : layout_dispatch_kernel<false>,
                       dim3(grid), dim3(kLDThreads), smem, stream, topk_idx, (int)T, k, E, R_cols,
