@@ -417,11 +417,13 @@ def run_ours(args, rank, world, local):
     if args.fused and args.path != "direct":
         raise SystemExit("--fused applies to the direct path")
     if args.path == "two_stage":
-        if wl.payload != "bf16":
-            raise SystemExit("the two-stage path is BF16 only")
         cap = ep.rank_rows_bound(wl.T, wl.k, wl.R)
         rl = ep.rank_layout(idx, wl.E, wl.R)
-        rank_buf = torch.empty(cap, wl.H, dtype=torch.bfloat16, device=dev)
+        if wl.payload == "fp8":   # rank rows hold e4m3 codes and scales
+            rank_q = torch.empty(cap, wl.H, dtype=torch.uint8, device=dev)
+            rank_s = torch.empty(cap, wl.H // 128, dtype=torch.float32, device=dev)
+        else:
+            rank_buf = torch.empty(cap, wl.H, dtype=torch.bfloat16, device=dev)
         partial = torch.empty(cap, wl.H, dtype=torch.bfloat16, device=dev)
         rws = torch.empty(max(16, ep.load().ep_rank_layout_workspace_bytes(wl.T, wl.k, wl.E, wl.R)),
                           dtype=torch.uint8, device=dev)
@@ -433,8 +435,14 @@ def run_ours(args, rank, world, local):
         ep.rank_layout(idx, wl.E, wl.R, out=rl, workspace=rws)
         if ev:
             ev[1].record(stream)
-        ep.dispatch(x, rl.rank_dst_row, cap, recv=rank_buf, status=lay.status)
-        ep.expand(rank_buf, rl, lay.dst_row, wl.rows, recv=recv, status=lay.status)
+        if wl.payload == "fp8":
+            ep.dispatch_fp8(x, rl.rank_dst_row, cap, recv_q=rank_q, recv_scale=rank_s,
+                            status=lay.status)
+            ep.expand_fp8(rank_q, rank_s, rl, lay.dst_row, wl.rows, recv_q=recv_q,
+                          recv_scale=recv_s, status=lay.status)
+        else:
+            ep.dispatch(x, rl.rank_dst_row, cap, recv=rank_buf, status=lay.status)
+            ep.expand(rank_buf, rl, lay.dst_row, wl.rows, recv=recv, status=lay.status)
         if ev:
             ev[2].record(stream)
         ep.combine_partial(y, w, lay.dst_row, rl, cap, partial=partial, status=lay.status)
@@ -579,10 +587,11 @@ def run_ours(args, rank, world, local):
     if args.path == "two_stage":
         # each timed stage is two kernels; nr = rank rows the route fills
         nr = int(rl.rank_offsets[-1])
+        row = wl.H + wl.H // 32 if wl.payload == "fp8" else wl.H * 2  # bytes of a dispatched row
         alg = {
             "layout": 2 * Tk * 4 + Tk * 4 + 2 * Tk * 4 + nr * 4,
-            "dispatch": (wl.T * wl.H * 2 + nr * wl.H * 2 + Tk * 4)          # copy to ranks
-                        + (nr * wl.H * 2 + Tk * wl.H * 2 + 2 * Tk * 4),     # expansion
+            "dispatch": (wl.T * wl.H * 2 + nr * row + Tk * 4)               # copy to ranks
+                        + (nr * row + Tk * row + 2 * Tk * 4),               # expansion
             "combine": (Tk * wl.H * 2 + nr * wl.H * 2 + Tk * 12 + nr * 4)   # rank-local partials
                        + (nr * wl.H * 2 + wl.T * wl.H * 2 + Tk * 4),       # final reduce
         }
