@@ -182,6 +182,33 @@ def ncu_traffic(kernel, workload):
     return ent.get("dram_bytes_per_launch")
 
 
+def algorithmic_bytes(wl, path="direct", fused=False, rank_rows=0):
+    """Algorithmic HBM bytes of each timed part of a step: what the method
+    must read and write once.  Direct path: the layout reads the ids and
+    writes dst_row; dispatch reads x and writes k rows per token (FP8: codes
+    plus a 4-byte scale per 128 channels); combine reads k rows and writes
+    one per token.  `fused`: layout and dispatch timed as one call.  Two-stage
+    path (`rank_rows` rank rows filled): the copy to ranks plus the expansion,
+    and the rank-local partials plus the final reduce."""
+    Tk = wl.T * wl.k
+    row = wl.H + wl.H // 32 if wl.payload == "fp8" else wl.H * 2  # bytes of a dispatched row
+    if path == "two_stage":
+        nr = rank_rows
+        return {
+            "layout": 2 * Tk * 4 + Tk * 4 + 2 * Tk * 4 + nr * 4,
+            "dispatch": (wl.T * wl.H * 2 + nr * row + Tk * 4)               # copy to ranks
+                        + (nr * row + Tk * row + 2 * Tk * 4),               # expansion
+            "combine": (Tk * wl.H * 2 + nr * wl.H * 2 + Tk * 12 + nr * 4)   # rank-local partials
+                       + (nr * wl.H * 2 + wl.T * wl.H * 2 + Tk * 4),       # final reduce
+        }
+    alg = {"layout": 2 * Tk * 4,
+           "dispatch": wl.T * wl.H * 2 + Tk * row + Tk * 4,
+           "combine": Tk * wl.H * 2 + wl.T * wl.H * 2 + Tk * 8}
+    if fused:
+        return {"layout_dispatch": alg["layout"] + alg["dispatch"], "combine": alg["combine"]}
+    return alg
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -570,31 +597,13 @@ def run_ours(args, rank, world, local):
     ms_per_step = max_total_s * 1e3 / args.steps
 
     # ---- roofline of the dominant kernel (algorithmic bytes / event time)
-    Tk = wl.T * wl.k
-    alg = {
-        "layout": 2 * Tk * 4,
-        "dispatch": (wl.T * wl.H * 2 + Tk * wl.H * 2 + Tk * 4) if wl.payload == "bf16" else
-                    (wl.T * wl.H * 2 + Tk * (wl.H + wl.H // 32) + Tk * 4),
-        "combine": Tk * wl.H * 2 + wl.T * wl.H * 2 + Tk * 8,
-    }
     per_launch_ms = {"layout": lay_ms / args.steps, "dispatch": disp_ms / args.steps,
                      "combine": comb_ms / args.steps}
-    if args.fused:
-        # the fused call is timed as one: its bytes are the layout's and the dispatch's
-        alg = {"layout_dispatch": alg["layout"] + alg["dispatch"], "combine": alg["combine"]}
+    if args.fused:  # the fused call is timed as one
         per_launch_ms = {"layout_dispatch": (lay_ms + disp_ms) / args.steps,
                          "combine": comb_ms / args.steps}
-    if args.path == "two_stage":
-        # each timed stage is two kernels; nr = rank rows the route fills
-        nr = int(rl.rank_offsets[-1])
-        row = wl.H + wl.H // 32 if wl.payload == "fp8" else wl.H * 2  # bytes of a dispatched row
-        alg = {
-            "layout": 2 * Tk * 4 + Tk * 4 + 2 * Tk * 4 + nr * 4,
-            "dispatch": (wl.T * wl.H * 2 + nr * row + Tk * 4)               # copy to ranks
-                        + (nr * row + Tk * row + 2 * Tk * 4),               # expansion
-            "combine": (Tk * wl.H * 2 + nr * wl.H * 2 + Tk * 12 + nr * 4)   # rank-local partials
-                       + (nr * wl.H * 2 + wl.T * wl.H * 2 + Tk * 4),       # final reduce
-        }
+    alg = algorithmic_bytes(wl, args.path, args.fused,
+                            int(rl.rank_offsets[-1]) if args.path == "two_stage" else 0)
     dominant = max((n for n in per_launch_ms if n != "layout"), key=lambda n: per_launch_ms[n])
     peak, peak_src = measured_peak()
     kname = "dispatch_fp8" if (dominant == "dispatch" and wl.payload == "fp8") else dominant

@@ -84,3 +84,29 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+def test_algorithmic_bytes_accounting():
+    sys.path.insert(0, ROOT)
+    import bench
+    from combine_ep_layout_02_gb300 import workloads as W
+    wl = W.WORKLOADS["prefill"]
+    T, H, k = wl.T, wl.H, wl.k
+    a = bench.algorithmic_bytes(wl)
+    assert a["layout"] == 2 * T * k * 4
+    assert a["dispatch"] == T * H * 2 + T * k * H * 2 + T * k * 4          # read x once, k rows out
+    assert a["combine"] == T * k * H * 2 + T * H * 2 + T * k * 8           # k rows in, one out
+    # the full-size prefill figures of the measurement table: 8,457.8 and 8,459.9 MB
+    assert round(a["dispatch"] / 1e6, 1) == 8457.8 and round(a["combine"] / 1e6, 1) == 8459.9
+    f = W.WORKLOADS["prefill_fp8"]
+    af = bench.algorithmic_bytes(f)
+    assert af["dispatch"] == f.T * f.H * 2 + f.T * f.k * (f.H + 4 * f.H // 128) + f.T * f.k * 4
+    assert round(af["dispatch"] / 1e6, 1) == 9634.3
+    fused = bench.algorithmic_bytes(wl, fused=True)
+    assert fused == {"layout_dispatch": a["layout"] + a["dispatch"], "combine": a["combine"]}
+    # two-stage with every pair in its own rank row equals the direct bytes plus
+    # one more write and read of those rows in each direction
+    nr = T * k
+    t2 = bench.algorithmic_bytes(wl, path="two_stage", rank_rows=nr)
+    assert t2["dispatch"] == a["dispatch"] + 2 * nr * H * 2 + 2 * T * k * 4
+    assert t2["combine"] == a["combine"] + 2 * nr * H * 2 + T * k * 8 + nr * 4
