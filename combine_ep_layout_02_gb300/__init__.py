@@ -10,5 +10,4 @@ from .binding import (  # noqa: F401
     layout_workspace_bytes, load,
     layout_static_ws, status_read, rank_layout, rank_rows_bound, expand, expand_fp8, combine_partial,
     combine_reduce, RankLayoutOut, EP_FLAG_BAD_EXPERT, EP_FLAG_OVERFLOW, EP_FLAG_BAD_ROW,
-    EP_FLAG_TIMEOUT,
 )

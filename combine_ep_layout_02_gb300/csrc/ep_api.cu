@@ -82,7 +82,7 @@ size_t ep_layout_workspace_bytes(int64_t T, int k, int E, int R, int with_rank_c
 
 }  // extern "C"
 
-namespace {
+namespace ep {
 
 // The host-side checks of ep_layout (EP_OK when the call may proceed).
 int check_layout_args(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
@@ -108,6 +108,12 @@ int check_layout_args(const int32_t* topk_idx, int64_t T, int k, int E, int R, i
     }
     return EP_OK;
 }
+
+}  // namespace ep
+
+namespace {
+
+using ep::check_layout_args;
 
 int layout_checked(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind, int capacity,
                    int align, int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,

@@ -9,17 +9,14 @@
 // one 8-warp block per SM, where this write-bound scatter is fastest.
 #include "ep_internal.cuh"
 
-#ifndef EP_DISPATCH_BULK
-#define EP_DISPATCH_BULK 0
-#endif
-#ifndef EP_BULK_STAGES
-#define EP_BULK_STAGES 4
-#endif
 #ifndef EP_DISPATCH_U
 #define EP_DISPATCH_U 4  // 16-byte vectors per lane in flight per row pass
 #endif
 #ifndef EP_DISPATCH_PREFETCH_MIN_TOKENS
 #define EP_DISPATCH_PREFETCH_MIN_TOKENS 16384  // batches this large use PREFETCH
+#endif
+#ifndef EP_DISPATCH_PERSISTENT
+#define EP_DISPATCH_PERSISTENT 0  // 1: large batches on a grid of one block per SM (slower)
 #endif
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
@@ -34,12 +31,17 @@ namespace {
 constexpr int kDispatchWarps = EP_DISPATCH_WARPS;  // warps per block
 constexpr int kRowRegs = 8;        // destination rows held in registers per pass
 
-// PREFETCH: the first pass's loads are issued before the destination rows
+// Units are (token, column slice) pairs, unit g = t * S + slice; warp w of
+// the grid takes units w, w + W, w + 2W, ... (W = warps in the grid), so the
+// same kernel serves a grid that covers every unit once and a persistent grid
+// of one block per SM.
+//
+// PREFETCH: a unit's first-pass loads are issued before its destination rows
 // are read, so the two latencies overlap (88 registers instead of 58).  Used
-// with the one-block-per-SM launch for large batches (65,536 tokens x 7168:
-// 1275 -> 1257 us at 2 blocks per SM, 1245 us at one); 1-2 % slower at 1,024
-// to 2,048 tokens and no faster below, so smaller batches use the plain
-// instance.  The same change in the FP8 dispatch measured 0.15 % slower.
+// with the persistent launch for large batches (65,536 tokens x 7168: 1275 ->
+// 1257 us at 2 blocks per SM, 1245 us at one); 1-2 % slower at 1,024 to 2,048
+// tokens and no faster below, so smaller batches use the plain instance.  The
+// same change in the FP8 dispatch measured 0.15 % slower.
 template <int U, bool PREFETCH>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k, int S,
@@ -48,49 +50,52 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
-    const int64_t t = slice_row(g, S);
-    if (t >= T) return;  // warp-uniform
-    const int64_t vb = (g - t * S) * slice;          // this warp's column slice [vb, ve)
-    const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
-    const uint4* src = x + t * nvec;
-    // the first pass's loads do not depend on the destination rows: issue
-    // them before the rows are read, so the two latencies overlap
-    uint4 first[U];
-    if (PREFETCH) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = vb + u * 32 + lane;
-            if (v < ve) first[u] = ld_stream_v4(src + v);
-        }
-    }
-    const int my_row = load_dst_row(dst_row, t, k, rows, status);
-    // k <= 8 is one pass; larger k re-reads the slice once per 8 destinations
-    for (int j0 = 0; j0 < k; j0 += kRowRegs) {
-        uint4* dst[kRowRegs];
-#pragma unroll
-        for (int jj = 0; jj < kRowRegs; ++jj) {
-            const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
-            dst[jj] = (j0 + jj < k && r >= 0) ? recv + (int64_t)r * nvec : nullptr;
-        }
-        for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
-            uint4 buf[U];
-            const bool pre = PREFETCH && j0 == 0 && v0 == vb;  // warp-uniform
+    const int64_t nunits = T * S;
+    const int64_t stride = (int64_t)gridDim.x * kDispatchWarps;
+    for (int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5); g < nunits;
+         g += stride) {  // warp-uniform
+        const int64_t t = slice_row(g, S);
+        const int64_t vb = (g - t * S) * slice;  // this warp's column slice [vb, ve)
+        const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
+        const uint4* src = x + t * nvec;
+        // the first pass's loads do not depend on the destination rows: issue
+        // them before the rows are read, so the two latencies overlap
+        uint4 first[U];
+        if (PREFETCH) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * 32 + lane;
-                if (pre) buf[u] = first[u];
-                else if (v < ve) buf[u] = ld_stream_v4(src + v);
+                const int64_t v = vb + u * 32 + lane;
+                if (v < ve) first[u] = ld_stream_v4(src + v);
             }
+        }
+        const int my_row = load_dst_row(dst_row, t, k, rows, status);
+        // k <= 8 is one pass; larger k re-reads the slice once per 8 destinations
+        for (int j0 = 0; j0 < k; j0 += kRowRegs) {
+            uint4* dst[kRowRegs];
 #pragma unroll
             for (int jj = 0; jj < kRowRegs; ++jj) {
-                if (dst[jj] == nullptr) continue;  // warp-uniform
+                const int r = __shfl_sync(kFullMask, my_row, (j0 + jj) & 31);
+                dst[jj] = (j0 + jj < k && r >= 0) ? recv + (int64_t)r * nvec : nullptr;
+            }
+            for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
+                uint4 buf[U];
+                const bool pre = PREFETCH && j0 == 0 && v0 == vb;  // warp-uniform
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t v = v0 + u * 32 + lane;
-                    if (v < ve) {
-                        if (EP_DISPATCH_STORE_CS) st_cs_v4(dst[jj] + v, buf[u]);
-                        else st_v4(dst[jj] + v, buf[u]);
+                    if (pre) buf[u] = first[u];
+                    else if (v < ve) buf[u] = ld_stream_v4(src + v);
+                }
+#pragma unroll
+                for (int jj = 0; jj < kRowRegs; ++jj) {
+                    if (dst[jj] == nullptr) continue;  // warp-uniform
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int64_t v = v0 + u * 32 + lane;
+                        if (v < ve) {
+                            if (EP_DISPATCH_STORE_CS) st_cs_v4(dst[jj] + v, buf[u]);
+                            else st_v4(dst[jj] + v, buf[u]);
+                        }
                     }
                 }
             }
@@ -98,75 +103,9 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
     }
 }
 
-// Bulk-copy (TMA engine) dispatch: persistent blocks of one warp; block b
-// handles tokens b, b + G, b + 2G, ...  A ring of S shared-memory stages holds
-// whole token rows: lane 0 loads a row with one cp.async.bulk completing on the
-// stage's mbarrier, then lane j (< k) writes it to destination row j with one
-// bulk store.  Loads run up to S-1 tokens ahead; a stage is refilled once the
-// stores of the token that used it have finished reading it.
-template <int S>
-__global__ void __launch_bounds__(32)
-dispatch_bf16_bulk_kernel(const uint8_t* __restrict__ x, int64_t T, uint32_t row_bytes, int k,
-                          const int32_t* __restrict__ dst_row, uint8_t* __restrict__ recv,
-                          int64_t rows, uint32_t* __restrict__ status) {
-    extern __shared__ __align__(128) uint8_t stage_mem[];
-    __shared__ __align__(8) uint64_t bar[S];
-    const int lane = threadIdx.x;
-    const int64_t G = gridDim.x;
-    const int64_t b = blockIdx.x;
-    const int64_t ntok = b < T ? (T - b + G - 1) / G : 0;
-
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    pdl_wait();
-    pdl_trigger();
-    if (ntok == 0) return;
-
-    auto load = [&](int64_t i) {  // lane 0 only
-        const int s = (int)(i % S);
-        mbar_arrive_expect_tx(&bar[s], row_bytes);
-        bulk_g2s(stage_mem + (size_t)s * row_bytes, x + (b + i * G) * (int64_t)row_bytes,
-                 row_bytes, &bar[s]);
-    };
-    if (lane == 0)
-        for (int64_t i = 0; i < S && i < ntok; ++i) load(i);
-
-    int my_row = load_dst_row(dst_row, b, k, rows, status);
-    bool timed_out = false;
-    for (int64_t i = 0; i < ntok; ++i) {
-        const int s = (int)(i % S);
-        const uint32_t parity = (uint32_t)((i / S) & 1);
-        const int next_row =
-            (i + 1 < ntok) ? load_dst_row(dst_row, b + (i + 1) * G, k, rows, status) : -1;
-        if (!mbar_wait_bounded(&bar[s], parity)) timed_out = true;
-        if (__any_sync(kFullMask, timed_out)) {
-            timed_out = true;
-            break;
-        }
-        if (lane < k) {
-            if (my_row >= 0)
-                bulk_s2g(recv + (int64_t)my_row * row_bytes, stage_mem + (size_t)s * row_bytes,
-                         row_bytes);
-            bulk_commit();  // one group per lane per token, possibly empty
-        }
-        // refill the stage of token i-1 with token i-1+S once its stores have
-        // read it (each lane's most recent group, token i, may still be pending)
-        if (i >= 1 && i - 1 + S < ntok) {
-            if (lane < k) bulk_wait_read<1>();
-            __syncwarp();
-            if (lane == 0) load(i - 1 + S);
-        }
-        my_row = next_row;
-    }
-    if (lane < k) bulk_wait_all();
-    if (timed_out && lane == 0 && status) atomicOr(status, EP_FLAG_TIMEOUT);
-}
-
 // Dynamic shared memory that admits one block per SM: just over half of an
-// SM's shared memory (0, no request, if the device reports too little).
+// SM's shared memory (0, no request, if the device reports too little).  The
+// kernel does not use it; the request only limits residency.
 size_t dispatch_occupancy_smem() {
     static std::atomic<int> per_sm_cache[64], per_block_cache[64];
     const int per_sm =
@@ -183,29 +122,6 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
                                  const int32_t* dst_row, void* recv, int64_t rows,
                                  uint32_t* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-#if EP_DISPATCH_BULK
-    {
-        constexpr int S = EP_BULK_STAGES;
-        const uint32_t row_bytes = (uint32_t)(H * 2);
-        const size_t smem = (size_t)S * row_bytes;
-        if (k <= 32 && smem <= 200 * 1024) {
-            auto kern = dispatch_bf16_bulk_kernel<S>;
-            cudaError_t e =
-                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            int dev = 0, sms = 0, per_sm = 0;
-            cudaGetDevice(&dev);
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32, smem);
-            if (e != cudaSuccess) return e;
-            const int64_t want = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
-            const unsigned grid = (unsigned)(T < want ? T : want);
-            return launch_pdl(kern, dim3(grid), dim3(32), smem, stream,
-                              static_cast<const uint8_t*>(x), T, row_bytes, k, dst_row,
-                              static_cast<uint8_t*>(recv), rows, status);
-        }
-    }
-#endif
     const int64_t nvec = H / 8;
     const RowSlices sl = row_slices(T, nvec);
     const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
@@ -214,19 +130,30 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
                           dim3(kDispatchWarps * 32), 0, stream, static_cast<const uint4*>(x), T,
                           nvec, k, sl.S, sl.slice, dst_row, static_cast<uint4*>(recv), rows,
                           status);
-    // Large batches: at most one 8-warp block per SM.  A write-bound scatter
-    // into k rows per token measured fastest with 8 warps per SM (65,536 x
-    // 7168: 1257 us at 16 warps, 1245 us at 8, 1403 us at 4), which the
-    // block's dynamic shared-memory request enforces (it is not otherwise
-    // used): more than half an SM's shared memory admits one block per SM.
+    // Large batches: at most one 8-warp block resident per SM.  A write-bound
+    // scatter into k rows per token measured fastest with 8 warps per SM
+    // (65,536 x 7168: 1257 us at 16 warps, 1245 us at 8, 1403 us at 4).  The
+    // residency limit is set by the block's dynamic shared-memory request
+    // (more than half of an SM's shared memory, which the kernel does not
+    // use).  A persistent grid of one block per SM looping over the tokens
+    // (EP_DISPATCH_PERSISTENT=1) measured slower: 1408 us against 1263 us
+    // with the same residency limit, 1422 us without it.
     auto kern = dispatch_bf16_kernel<EP_DISPATCH_U, true>;
+    unsigned pgrid = grid;
+#if EP_DISPATCH_PERSISTENT
+    {
+        static std::atomic<int> sm_cache[64];
+        const int sms = cached_device_attribute(cudaDevAttrMultiProcessorCount, sm_cache);
+        if (sms > 0 && (unsigned)sms < grid) pgrid = (unsigned)sms;
+    }
+#endif
     const size_t smem = dispatch_occupancy_smem();
     if (smem > 0) {
         static std::atomic<uint64_t> configured{0};
         const cudaError_t e = raise_smem_limit(kern, smem, configured);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kDispatchWarps * 32), smem, stream,
+    return launch_pdl(kern, dim3(pgrid), dim3(kDispatchWarps * 32), smem, stream,
                       static_cast<const uint4*>(x), T, nvec, k, sl.S, sl.slice, dst_row,
                       static_cast<uint4*>(recv), rows, status);
 }

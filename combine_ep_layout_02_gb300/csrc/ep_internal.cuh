@@ -95,91 +95,6 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ---- bulk (TMA engine) copies and mbarriers -------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-// Make mbarrier initialisation visible to the async (TMA) proxy.
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-// One bounded probe of phase `parity`; true once that phase has completed.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Global -> shared bulk copy completing on `bar` (bytes % 16 == 0, both
-// addresses 16-byte aligned).
-__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
-                                         uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(smem_dst)),
-        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Shared -> global bulk copy tracked by this thread's bulk async-groups.
-__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
-                 "r"(smem_u32(smem_src)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until at most N of this thread's bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Wait until all of this thread's bulk groups have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Longest a kernel waits for one of its own copies before it gives up, flags
-// EP_FLAG_TIMEOUT and returns.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
-// Wait for phase `parity` of `bar`, for at most kWaitLimitNs; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
 // OR device-side condition bits into the optional status word: one atomic
 // per warp at most.
 __device__ __forceinline__ void warp_flag(uint32_t* status, bool cond, uint32_t bit) {
@@ -420,6 +335,13 @@ struct RowSlices {
     int64_t slice;  // 16-byte vectors per slice
 };
 RowSlices row_slices(int64_t T, int64_t nvec);
+
+// The host-side argument checks of ep_layout (EP_OK when the call may
+// proceed); `workspace` / `workspace_bytes` are what the layout would use.
+int check_layout_args(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
+                      int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
+                      int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
+                      void* workspace, size_t workspace_bytes);
 
 // Tokens per layout chunk (one per thread of a 128-thread block).
 constexpr int kLayoutThreads = 128;

@@ -44,8 +44,16 @@ extern "C" int ep_layout_static_ws(const int32_t* topk_idx, int64_t T, int k, in
                                    int kind, int capacity, int32_t* expert_counts,
                                    int32_t* expert_offsets, int32_t* dst_row,
                                    int32_t* rank_token_counts, uint32_t* status, void* stream) {
+    // the checks of ep_layout first, against the fixed array's size, so that
+    // both calls report a bad argument the same way; a size beyond the array
+    // gives EP_ERR_WORKSPACE.  The placeholder pointer stands for the array
+    // (aligned, never dereferenced on the host).
+    void* const placeholder = reinterpret_cast<void*>(static_cast<uintptr_t>(256));
+    const int rc = ep::check_layout_args(topk_idx, T, k, E, R, kind, capacity, 1, expert_counts,
+                                         expert_offsets, dst_row, rank_token_counts, status,
+                                         placeholder, (size_t)EP_STATIC_WS_BYTES);
+    if (rc != EP_OK) return rc;
     const size_t need = ep_layout_workspace_bytes(T, k, E, R, rank_token_counts != nullptr);
-    if (need > (size_t)EP_STATIC_WS_BYTES) return EP_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0) {
         const int err = scratch_address(&scratch);

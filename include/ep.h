@@ -79,9 +79,7 @@ typedef enum {
 enum {
     EP_FLAG_BAD_EXPERT = 1u, /* an expert id outside [-1, E): the pair was skipped */
     EP_FLAG_OVERFLOW = 2u,   /* masked layout: slot >= capacity, the pair was dropped */
-    EP_FLAG_BAD_ROW = 4u,    /* dispatch/combine: dst_row outside [-1, rows): skipped */
-    EP_FLAG_TIMEOUT = 8u     /* a bounded wait for an in-flight copy gave up: output
-                                incomplete (only the optional bulk-copy dispatch build waits) */
+    EP_FLAG_BAD_ROW = 4u     /* dispatch/combine: dst_row outside [-1, rows): skipped */
 };
 
 typedef enum { EP_LAYOUT_CONTIGUOUS = 0, EP_LAYOUT_MASKED = 1 } ep_layout_kind_t;
@@ -171,7 +169,11 @@ EP_API int ep_layout_aligned(const int32_t* topk_idx, int64_t T, int k, int E, i
  *  - The first call on a device looks up the array's device address, with
  *    the caller's current device; that device must be the one `stream`
  *    belongs to.  Make the first call on each device before any stream
- *    capture begins.
+ *    capture begins.  The address is kept for the life of the process:
+ *    cudaDeviceReset() (or anything else that destroys the device's primary
+ *    context) between calls is not supported.
+ *  - Argument errors are reported as ep_layout() reports them; a size beyond
+ *    the array's limit then gives EP_ERR_WORKSPACE.
  *  - Every call on a device shares the one array, and it keeps the last
  *    call's contents (the layout fully rewrites what it reads, so nothing
  *    needs clearing).  Calls whose kernels overlap on the GPU (for example

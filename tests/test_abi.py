@@ -47,7 +47,7 @@ def test_binding_constants_match_the_header():
     with open(os.path.join(ROOT, "include", "ep.h")) as f:
         text = f.read()
     consts = dict(re.findall(r"\b(EP_(?:FLAG|ERR|OK)\w*)\s*=\s*(\d+)u?\b", text))
-    assert {"EP_FLAG_BAD_EXPERT", "EP_FLAG_OVERFLOW", "EP_FLAG_BAD_ROW", "EP_FLAG_TIMEOUT",
+    assert {"EP_FLAG_BAD_EXPERT", "EP_FLAG_OVERFLOW", "EP_FLAG_BAD_ROW",
             "EP_ERR_INVALID_ARG", "EP_ERR_ALIGNMENT", "EP_ERR_WORKSPACE", "EP_ERR_CUDA"} <= set(consts)
     for name, value in consts.items():
         assert getattr(binding, name) == int(value), name

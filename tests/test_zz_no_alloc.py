@@ -33,7 +33,14 @@ def _same(a, b):
 
 def test_static_scratch_layout_matches_workspace_layout_twice():
     dev = torch.device("cuda:0")
-    cases = [W.WORKLOADS["prefill_fp8"], W.WORKLOADS["decode_fp8"]]   # large then small: stale scratch must not leak
+    # Both chunked-path cases use the scratch; the second has fewer chunks and
+    # fewer columns (72 x 32 against 288 x 1024 int32 counters), so the first
+    # call's counters are still in the array at other positions and any entry
+    # the second call failed to rewrite would be read stale.  decode_fp8 takes
+    # the one-launch path, which needs no scratch.
+    cases = [W.WORKLOADS["prefill_fp8"],
+             W.WORKLOADS["prefill"].scaled(T=4096, E=64, R=8),
+             W.WORKLOADS["decode_fp8"]]
     for wl in cases:
         idx = W.route(wl, device=dev)
         for _ in range(2):                                            # two calls in a row
@@ -52,3 +59,13 @@ def test_static_scratch_rejects_sizes_beyond_its_limit():
     assert need > (2 << 20)
     rc = lib.ep_layout_static_ws(fake, T, k, E, R, 0, 0, fake, fake, fake, fake, None, None)
     assert rc == binding.EP_ERR_WORKSPACE
+
+
+def test_static_scratch_reports_bad_arguments_like_ep_layout():
+    lib = binding.load()
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the call is rejected on the host
+    T, k, E, R = 1 << 20, 8, 2048, 1024          # E above EP_MAX_EXPERTS, and too large for the array
+    rc = lib.ep_layout_static_ws(fake, T, k, E, R, 0, 0, fake, fake, fake, fake, None, None)
+    assert rc == binding.EP_ERR_INVALID_ARG
+    rc = lib.ep_layout(fake, T, k, E, R, 0, 0, fake, fake, fake, fake, None, fake, 1 << 30, None)
+    assert rc == binding.EP_ERR_INVALID_ARG
