@@ -94,7 +94,8 @@ WORKLOADS = {
                                       "within 4 ranks (at least 2 pairs per rank copy)"),
 }
 
-_STREAMS = {"x": 1, "route": 2, "logits": 3, "y": 4, "scale": 5, "outliers": 6}
+_STREAMS = {"x": 1, "route": 2, "logits": 3, "y": 4, "scale": 5, "outliers": 6,
+            "y_q": 7, "y_scale": 8}
 
 
 def _gen(seed, stream, device):
@@ -194,6 +195,25 @@ def independent_expert_outputs(wl, device="cpu", chunk_rows=8192):
         y[r0:r1] = torch.randn(r1 - r0, wl.H, generator=g, device=device,
                                dtype=torch.float32).to(torch.bfloat16)
     return y
+
+
+def fp8_expert_outputs(wl, device="cpu", chunk_rows=8192):
+    """Expert outputs already in the FP8 payload encoding, for the FP8
+    combine: codes y_q [rows, H] uint8 drawn uniformly from the 254 finite
+    e4m3 codes (0x7F and 0xFF, the NaN codes, excluded), and one float32
+    scale per row and 128 channels, y_scale [rows, H/128] = (2 + U(0,2)) / 448
+    (the scale of a block whose largest magnitude is 2..4, as N(0,1) rows
+    give).  Plain random draws: no quantisation happens here."""
+    g = _gen(wl.seed, "y_q", device)
+    gs = _gen(wl.seed, "y_scale", device)
+    q = torch.empty(wl.rows, wl.H, dtype=torch.uint8, device=device)
+    for r0 in range(0, wl.rows, chunk_rows):
+        r1 = min(wl.rows, r0 + chunk_rows)
+        c = torch.randint(0, 254, (r1 - r0, wl.H), generator=g, device=device, dtype=torch.int32)
+        q[r0:r1] = (c + (c >= 127).to(torch.int32)).to(torch.uint8)   # skip 0x7F
+    sc = (2.0 + 2.0 * torch.rand(wl.rows, wl.H // 128, generator=gs, device=device,
+                                 dtype=torch.float32)) / 448.0
+    return q, sc
 
 
 def scale_rows(recv, row_expert, scales):

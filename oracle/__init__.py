@@ -58,6 +58,10 @@ def _load():
         lib.oracle_quantize_row_fp8.restype = None
         lib.oracle_dispatch_fp8.argtypes = [P, i64, i64, i32, P, P, P]
         lib.oracle_dispatch_fp8.restype = None
+        lib.oracle_combine_fp8_f64.argtypes = [P, P, P, P, i64, i64, i32, P, P, P]
+        lib.oracle_combine_fp8_f64.restype = None
+        lib.oracle_combine_fp8_fp32_seq.argtypes = [P, P, P, P, i64, i64, i32, P]
+        lib.oracle_combine_fp8_fp32_seq.restype = None
         lib.oracle_combine_f64.argtypes = [P, P, P, i64, i64, i32, P, P, P]
         lib.oracle_combine_f64.restype = None
         lib.oracle_combine_fp32_seq.argtypes = [P, P, P, i64, i64, i32, P]
@@ -197,6 +201,37 @@ def combine_fp32_seq(y, topk_w, dst_row):
 
 
 # --- two-stage (rank, then expert) path ------------------------------------
+
+def combine_fp8_f64(y_q, y_scale, topk_w, dst_row):
+    """Combine of FP8 expert outputs (codes [rows,H], scales [rows,H/128]).
+    Returns (out uint16 [T,H], ref float64 [T,H], absum float64 [T,H])."""
+    q = _c(y_q, np.uint8)
+    sc = _c(y_scale, np.float32)
+    w = _c(topk_w, np.float32)
+    dst = _c(dst_row, np.int32)
+    T, k = dst.shape
+    H = q.shape[1]
+    out = np.zeros((T, H), np.uint16)
+    ref = np.zeros((T, H), np.float64)
+    absum = np.zeros((T, H), np.float64)
+    _load().oracle_combine_fp8_f64(_p(q), _p(sc), _p(w), _p(dst), T, H, k, _p(out), _p(ref),
+                                   _p(absum))
+    return out, ref, absum
+
+
+def combine_fp8_fp32_seq(y_q, y_scale, topk_w, dst_row):
+    """The FP8 combine in fp32 (coefficient w*scale, then an FMA chain in j
+    order), rounded to bf16: uint16 [T,H]."""
+    q = _c(y_q, np.uint8)
+    sc = _c(y_scale, np.float32)
+    w = _c(topk_w, np.float32)
+    dst = _c(dst_row, np.int32)
+    T, k = dst.shape
+    H = q.shape[1]
+    out = np.zeros((T, H), np.uint16)
+    _load().oracle_combine_fp8_fp32_seq(_p(q), _p(sc), _p(w), _p(dst), T, H, k, _p(out))
+    return out
+
 
 def rank_layout(topk_idx, E, R):
     """Returns dict(rank_counts, rank_offsets, rank_dst_row, pair_rank_row,

@@ -320,6 +320,67 @@ void oracle_combine_fp32_seq(const uint16_t* y, const float* topk_w,
     }
 }
 
+/* Combine of expert outputs held in FP8.  The PR's review (section 9,
+ * "Smaller notes") names a compressed combine path without defining it, and
+ * its B300 re-run keeps combine in BF16 in both payload modes, so the pages
+ * fix no formula.  Reading taken: the expert outputs carry the same encoding
+ * as the FP8 dispatch payload -- e4m3 codes y_q[rows, H] and one float32
+ * scale y_scale[rows, H/128] per 128 channels, the value of a code being
+ * decode(q) * scale (the dequantisation of the dispatch recipe) -- and the
+ * combine is the BF16 combine applied to those values:
+ *   out[t,h] = bf16( sum_j [dst_row != -1] w[t,j] * decode(q[r,h]) * s[r,h/128] ).
+ * A float32 weight (24 significant bits) times a float32 scale (24) times a
+ * decoded e4m3 value (at most 4) has at most 52 significant bits, so every
+ * product is exact in double; the sum is taken in double and rounded to bf16
+ * once.  A token with no valid pair gives +0. */
+void oracle_combine_fp8_f64(const uint8_t* y_q, const float* y_scale,
+                            const float* topk_w, const int32_t* dst_row,
+                            int64_t T, int64_t H, int k, uint16_t* out,
+                            double* ref, double* absum) {
+    int64_t nb = H / 128;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            double s = 0.0, sa = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = dst_row[t * k + j];
+                if (r < 0) continue;
+                double v = (double)oracle_e4m3_decode(y_q[(int64_t)r * H + h]) *
+                           (double)y_scale[(int64_t)r * nb + h / 128];
+                double p = (double)topk_w[t * k + j] * v;
+                s += p;
+                sa += fabs(p);
+            }
+            if (out) out[t * H + h] = oracle_bf16_from_double(s);
+            if (ref) ref[t * H + h] = s;
+            if (absum) absum[t * H + h] = sa;
+        }
+    }
+}
+
+/* The same combine in fp32 arithmetic, in the order a streaming kernel can
+ * use: for each valid pair j (increasing) and 128-channel block b the
+ * coefficient c = fl32(w[t,j] * s[r,b]) (one rounding), then
+ * acc = fmaf(c, decode(q[r,h]), acc) (one rounding per step), and the final
+ * fp32 sum rounded to bf16.  Within (k + 1) * 2^-24 * sum_j |w*v| of the
+ * fp64 sum before the bf16 rounding. */
+void oracle_combine_fp8_fp32_seq(const uint8_t* y_q, const float* y_scale,
+                                 const float* topk_w, const int32_t* dst_row,
+                                 int64_t T, int64_t H, int k, uint16_t* out) {
+    int64_t nb = H / 128;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = dst_row[t * k + j];
+                if (r < 0) continue;
+                float c = topk_w[t * k + j] * y_scale[(int64_t)r * nb + h / 128];
+                acc = fmaf(c, oracle_e4m3_decode(y_q[(int64_t)r * H + h]), acc);
+            }
+            out[t * H + h] = oracle_bf16_from_double((double)acc);
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Two-stage path: one copy per (token, virtual rank), then expansion into  */
 /* the experts of that rank; rank-local partial sums, then a final sum.     */

@@ -77,6 +77,21 @@ void oracle_combine_fp32_seq(const uint16_t* y, const float* topk_w,
                              const int32_t* dst_row, int64_t T, int64_t H,
                              int k, uint16_t* out);
 
+/* Combine of FP8 expert outputs: codes y_q [rows,H], scales y_scale
+ * [rows,H/128] (value = decode(q) * scale).  out[t,h] = bf16 of the fp64 sum
+ * of w[t,j] * value over the valid pairs (every product exact in double);
+ * ref / absum as for oracle_combine_f64 (may be NULL). */
+void oracle_combine_fp8_f64(const uint8_t* y_q, const float* y_scale,
+                            const float* topk_w, const int32_t* dst_row,
+                            int64_t T, int64_t H, int k, uint16_t* out,
+                            double* ref, double* absum);
+
+/* The same in fp32: c = fl32(w * scale) per pair and block, then fmaf(c,
+ * decode(q), acc) in increasing j, then one rounding to bf16. */
+void oracle_combine_fp8_fp32_seq(const uint8_t* y_q, const float* y_scale,
+                                 const float* topk_w, const int32_t* dst_row,
+                                 int64_t T, int64_t H, int k, uint16_t* out);
+
 /* ---- two-stage (rank, then expert) path ---------------------------------
  * Rank layout: every (token t, virtual rank r) that t reaches gets one row of
  * a rank buffer, rank r's rows in token order.  rank_dst_row[t,j] is that row
