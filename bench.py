@@ -43,6 +43,7 @@ KERNEL_SOURCES = {
     "dispatch": "combine_ep_layout_02_gb300/csrc/ep_dispatch.cu",
     "dispatch_fp8": "combine_ep_layout_02_gb300/csrc/ep_dispatch_fp8.cu",
     "combine": "combine_ep_layout_02_gb300/csrc/ep_combine.cu",
+    "combine_fp8": "combine_ep_layout_02_gb300/csrc/ep_combine_fp8.cu",
 }
 
 
@@ -77,6 +78,9 @@ def parse():
                     help="time only the routing layout (20 calls captured in one CUDA graph)")
     ap.add_argument("--fused", action="store_true",
                     help="layout + dispatch through ep_layout_dispatch (one launch up to 128 tokens)")
+    ap.add_argument("--combine", default="bf16", choices=["bf16", "fp8"],
+                    help="fp8: expert outputs held as e4m3 codes + per-128-channel scales, "
+                         "combined by ep_combine_fp8")
     ap.add_argument("--graph", action="store_true",
                     help="replay the step as one captured CUDA graph (launch-bound small shapes)")
     return ap.parse_args()
@@ -182,12 +186,13 @@ def ncu_traffic(kernel, workload):
     return ent.get("dram_bytes_per_launch")
 
 
-def algorithmic_bytes(wl, path="direct", fused=False, rank_rows=0):
+def algorithmic_bytes(wl, path="direct", fused=False, rank_rows=0, combine="bf16"):
     """Algorithmic HBM bytes of each timed part of a step: what the method
     must read and write once.  Direct path: the layout reads the ids and
     writes dst_row; dispatch reads x and writes k rows per token (FP8: codes
     plus a 4-byte scale per 128 channels); combine reads k rows and writes
-    one per token.  `fused`: layout and dispatch timed as one call.  Two-stage
+    one per token (FP8 expert outputs: codes plus a 4-byte scale per 128
+    channels).  `fused`: layout and dispatch timed as one call.  Two-stage
     path (`rank_rows` rank rows filled): the copy to ranks plus the expansion,
     and the rank-local partials plus the final reduce."""
     Tk = wl.T * wl.k
@@ -201,9 +206,10 @@ def algorithmic_bytes(wl, path="direct", fused=False, rank_rows=0):
             "combine": (Tk * wl.H * 2 + nr * wl.H * 2 + Tk * 12 + nr * 4)   # rank-local partials
                        + (nr * wl.H * 2 + wl.T * wl.H * 2 + Tk * 4),       # final reduce
         }
+    in_row = wl.H + wl.H // 32 if combine == "fp8" else wl.H * 2  # bytes of an expert-output row
     alg = {"layout": 2 * Tk * 4,
            "dispatch": wl.T * wl.H * 2 + Tk * row + Tk * 4,
-           "combine": Tk * wl.H * 2 + wl.T * wl.H * 2 + Tk * 8}
+           "combine": Tk * in_row + wl.T * wl.H * 2 + Tk * 8}
     if fused:
         return {"layout_dispatch": alg["layout"] + alg["dispatch"], "combine": alg["combine"]}
     return alg
@@ -258,11 +264,27 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- oracle timing
 
-def oracle_sample(wl, x_host_bits, idx_host, w_host, tokens, seconds):
+def host_cpu():
+    """Cores and model of the host CPU (for the CPU-baseline record)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    import platform
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.processor() or None,
+            "machine": platform.machine()}
+
+
+def oracle_sample(wl, x_host_bits, idx_host, w_host, tokens, seconds, combine="bf16"):
     """Time the CPU oracle (layout + dispatch + combine of the first `tokens`
     tokens) in repeated passes until `seconds` elapse; return logical GB/s and
     details.  The expert outputs combined are the dispatched BF16 rows, built
-    once outside the timed passes."""
+    once outside the timed passes (FP8 combine: seeded codes and scales)."""
     import oracle
     T = min(tokens, wl.T)
     idx = idx_host[:T]
@@ -275,6 +297,9 @@ def oracle_sample(wl, x_host_bits, idx_host, w_host, tokens, seconds):
     disp_b, comb_b = sub.logical_bytes()
     lay0 = oracle.layout(idx, wl.E, wl.R, kind, cap)
     y = oracle.dispatch_bf16(xb, lay0["dst_row"], rows)
+    if combine == "fp8":
+        yq, ys = W.fp8_expert_outputs(sub)
+        yq, ys = yq.numpy(), ys.numpy()
     passes, t_lay, t_disp, t_comb = 0, 0.0, 0.0, 0.0
     t0 = time.perf_counter()
     while True:
@@ -286,7 +311,10 @@ def oracle_sample(wl, x_host_bits, idx_host, w_host, tokens, seconds):
         else:
             oracle.dispatch_bf16(xb, lay["dst_row"], rows)
         c = time.perf_counter()
-        oracle.combine_f64(y, w, lay["dst_row"])
+        if combine == "fp8":
+            oracle.combine_fp8_f64(yq, ys, w, lay["dst_row"])
+        else:
+            oracle.combine_f64(y, w, lay["dst_row"])
         d = time.perf_counter()
         passes += 1
         t_lay, t_disp, t_comb = t_lay + b - a, t_disp + c - b, t_comb + d - c
@@ -299,11 +327,13 @@ def oracle_sample(wl, x_host_bits, idx_host, w_host, tokens, seconds):
         "cores": 1,
         "kind": "oracle",
         "sample": "%d passes of layout+dispatch+combine over the first %d of %d tokens "
-                  "(%.1f s, single-threaded C)" % (passes, T, wl.T, total),
+                  "(%.1f s, single-threaded C; time.perf_counter around each step)" % (
+                      passes, T, wl.T, total),
         "us_per_call": total / passes * 1e6,
         "us_layout": t_lay / passes * 1e6,
         "us_dispatch": t_disp / passes * 1e6,
         "us_combine": t_comb / passes * 1e6,
+        **host_cpu(),
     }
 
 
@@ -322,11 +352,11 @@ def run_reference(args, rank, world):
     idx = W.route(sub).numpy()
     w = W.topk_weights(sub).numpy()
     for _ in range(args.warmup):
-        oracle_sample(wl, x, idx, w, tokens, 0.0)
+        oracle_sample(wl, x, idx, w, tokens, 0.0, args.combine)
     vals, secs = [], 0.0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = oracle_sample(wl, x, idx, w, tokens, 0.0)
+        r = oracle_sample(wl, x, idx, w, tokens, 0.0, args.combine)
         vals.append(r["us_per_call"])
     secs = time.perf_counter() - t0
     disp_b, comb_b = sub.logical_bytes()
@@ -339,11 +369,11 @@ def run_reference(args, rank, world):
         "data": "synthetic",
         "config": {"workload": wl.name, "T_sampled": tokens, "T": wl.T, "H": wl.H, "E": wl.E,
                    "k": wl.k, "R": wl.R, "layout": wl.kind, "payload": wl.payload,
-                   "route": wl.route, "zipf_s": wl.zipf_s},
+                   "route": wl.route, "zipf_s": wl.zipf_s, "combine": args.combine},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "each step: layout+dispatch+combine of the first %d of %d "
                                    "tokens (single-threaded C oracle); %.1f s total" % (
-                                       tokens, wl.T, secs)},
+                                       tokens, wl.T, secs), **host_cpu()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -427,7 +457,15 @@ def run_ours(args, rank, world, local):
     recv = None
     if wl.payload == "bf16" or wl.expert_out == "recv":
         recv = torch.empty(wl.rows, wl.H, dtype=torch.bfloat16, device=dev)
-    if wl.expert_out == "recv":
+    y_q = y_s = None
+    if args.combine == "fp8":
+        if args.path != "direct":
+            raise SystemExit("--combine fp8 applies to the direct path")
+        # expert outputs in the FP8 payload encoding: independent draws of
+        # codes and per-128-channel scales (no bf16 expert outputs exist)
+        y_q, y_s = W.fp8_expert_outputs(wl, device=dev)
+        y = None
+    elif wl.expert_out == "recv":
         y = recv
     elif wl.expert_out == "independent":
         y = W.independent_expert_outputs(wl, device=dev)
@@ -504,7 +542,10 @@ def run_ours(args, rank, world, local):
                 ep.dispatch(x, lay.dst_row, wl.rows, recv=recv, status=lay.status)
             if ev:
                 ev[2].record(stream)
-        ep.combine(y, w, lay.dst_row, out=out, status=lay.status)
+        if y_q is not None:
+            ep.combine_fp8(y_q, y_s, w, lay.dst_row, out=out, status=lay.status)
+        else:
+            ep.combine(y, w, lay.dst_row, out=out, status=lay.status)
         if ev:
             ev[3].record(stream)
 
@@ -537,7 +578,8 @@ def run_ours(args, rank, world, local):
     # else L2 is flushed (a buffer twice its size is written) between steps
     l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
     elem = 1 if wl.payload == "fp8" else 2
-    touched = (x.numel() * 2 + wl.T * wl.k * wl.H * elem + wl.T * wl.k * wl.H * 2
+    celem = 1 if args.combine == "fp8" else 2
+    touched = (x.numel() * 2 + wl.T * wl.k * wl.H * elem + wl.T * wl.k * wl.H * celem
                + out.numel() * 2)
     flush = args.l2_flush or (touched < 4 * l2_bytes and not args.no_l2_flush)
     if flush:
@@ -603,10 +645,13 @@ def run_ours(args, rank, world, local):
         per_launch_ms = {"layout_dispatch": (lay_ms + disp_ms) / args.steps,
                          "combine": comb_ms / args.steps}
     alg = algorithmic_bytes(wl, args.path, args.fused,
-                            int(rl.rank_offsets[-1]) if args.path == "two_stage" else 0)
+                            int(rl.rank_offsets[-1]) if args.path == "two_stage" else 0,
+                            combine=args.combine)
     dominant = max((n for n in per_launch_ms if n != "layout"), key=lambda n: per_launch_ms[n])
     peak, peak_src = measured_peak()
     kname = "dispatch_fp8" if (dominant == "dispatch" and wl.payload == "fp8") else dominant
+    if dominant == "combine" and args.combine == "fp8":
+        kname = "combine_fp8"
     if args.path == "two_stage":
         kname = {"dispatch": "rank_copy+expand", "combine": "combine_partial+reduce"}[dominant]
 
@@ -636,7 +681,7 @@ def run_ours(args, rank, world, local):
     # layout, streams x in token chunks overlapped with dispatch + combine, and
     # streams the output back, all inside the timed region
     e2e = None
-    if not args.no_e2e and args.path == "direct":
+    if not args.no_e2e and args.path == "direct" and args.combine == "bf16":
         xh = x.cpu().pin_memory()
         ih = idx.cpu().pin_memory()
         wh = w.cpu().pin_memory()
@@ -676,7 +721,7 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tokens = 1024
         cpu = oracle_sample(wl, W.bf16_bits(x[:tokens]), idx[:tokens].cpu().numpy(),
-                            w[:tokens].cpu().numpy(), tokens, args.cpu_seconds)
+                            w[:tokens].cpu().numpy(), tokens, args.cpu_seconds, args.combine)
 
     if rank == 0:
         props = torch.cuda.get_device_properties(dev)
@@ -693,7 +738,7 @@ def run_ours(args, rank, world, local):
                        "parallelism": "replicas x%d" % world,
                        "launch": ("cuda graph" if args.graph else "stream (programmatic dependent launch)")
                                  + ("; layout+dispatch through ep_layout_dispatch" if args.fused else ""),
-                       "path": args.path},
+                       "path": args.path, "combine": args.combine},
             "roofline": roofline,
             "kernels": kernels,
             "cpu_baseline": cpu,

@@ -69,6 +69,7 @@ def load():
         "ep_layout_dispatch_fp8": ([P, i64, i32, i32, i32, i32, i32, P, i64, P, P, P, P, P, P,
                                     i64, P, P, sz, P], i32),
         "ep_combine": ([P, P, P, i64, i64, i32, i64, P, P, P], i32),
+        "ep_combine_fp8": ([P, P, P, P, i64, i64, i32, i64, P, P, P], i32),
         "ep_status_read": ([P, P, P], i32),
         "ep_pipeline_create": ([i32, ctypes.POINTER(ctypes.c_void_p)], i32),
         "ep_pipeline_destroy": ([P], i32),
@@ -294,6 +295,28 @@ def combine(y, topk_w, dst_row, out=None, status=None):
         code = load().ep_combine(_ptr(y), _ptr(topk_w), _ptr(dst_row), T, H, k, rows, _ptr(out),
                                  _ptr(status), _stream(y.device))
     _rc("ep_combine", code)
+    return out
+
+
+def combine_fp8(y_q, y_scale, topk_w, dst_row, out=None, status=None):
+    """Weighted top-k combine of FP8 expert outputs (codes ``y_q`` [rows, H]
+    uint8, scales ``y_scale`` [rows, H/128] float32) into ``out`` [T, H] bf16
+    (see ``ep_combine_fp8``)."""
+    _check_dev("y_q", y_q, torch.uint8)
+    _check_dev("y_scale", y_scale, torch.float32, y_q.device)
+    _check_dev("topk_w", topk_w, torch.float32, y_q.device)
+    _check_dev("dst_row", dst_row, torch.int32, y_q.device)
+    rows, H = y_q.shape
+    T, k = dst_row.shape
+    if tuple(y_scale.shape) != (rows, H // 128):
+        raise ValueError("y_scale must be [rows, H/128]")
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=y_q.device)
+    _check_dev("out", out, torch.bfloat16, y_q.device)
+    with _on(y_q.device):
+        code = load().ep_combine_fp8(_ptr(y_q), _ptr(y_scale), _ptr(topk_w), _ptr(dst_row), T, H,
+                                     k, rows, _ptr(out), _ptr(status), _stream(y_q.device))
+    _rc("ep_combine_fp8", code)
     return out
 
 

@@ -253,6 +253,21 @@ int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row, int64
                                           as_stream(stream)));
 }
 
+int ep_combine_fp8(const uint8_t* y_q, const float* y_scale, const float* topk_w,
+                   const int32_t* dst_row, int64_t T, int64_t H, int k, int64_t rows, void* out,
+                   uint32_t* status, void* stream) {
+    int rc = check_rows_args(T, H, k, rows);
+    if (rc != EP_OK) return rc;
+    if (H % 128 != 0) return EP_ERR_ALIGNMENT;
+    if (T == 0) return EP_OK;
+    if (!topk_w || !dst_row || !out || ((!y_q || !y_scale) && rows > 0)) return EP_ERR_INVALID_ARG;
+    if (!aligned(y_q, 16) || !aligned(y_scale, 4) || !aligned(out, 16) || !aligned(topk_w, 4) ||
+        !aligned(dst_row, 4) || !aligned(status, 4))
+        return EP_ERR_ALIGNMENT;
+    return cuda_status(ep::launch_combine_fp8(y_q, y_scale, topk_w, dst_row, T, H, k, rows, out,
+                                              status, as_stream(stream)));
+}
+
 size_t ep_rank_layout_workspace_bytes(int64_t T, int k, int E, int R) {
     if (T <= 0 || k < 1 || E < 1 || R < 1) return 0;
     return ep::rank_keys_bytes(T, k) + ep_layout_workspace_bytes(T, k, R, 1, 0);

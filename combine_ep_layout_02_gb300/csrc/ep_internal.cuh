@@ -378,6 +378,10 @@ cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* ds
                            int64_t H, int k, int64_t rows, void* out, uint32_t* status,
                            cudaStream_t stream);
 
+cudaError_t launch_combine_fp8(const uint8_t* y_q, const float* y_scale, const float* topk_w,
+                               const int32_t* dst_row, int64_t T, int64_t H, int k, int64_t rows,
+                               void* out, uint32_t* status, cudaStream_t stream);
+
 // two-stage (rank, then expert) path
 size_t rank_keys_bytes(int64_t T, int k);
 cudaError_t launch_rank_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R,

@@ -271,6 +271,28 @@ EP_API int ep_combine(const void* y, const float* topk_w, const int32_t* dst_row
                uint32_t* status, void* stream);
 
 /*
+ * ep_combine_fp8 -- the combine for expert outputs carried in the FP8
+ * payload's own encoding (PR #1238, review section 9 "Smaller notes", names a
+ * compressed combine path but fixes no format; this is the reading taken):
+ * e4m3 codes and one float32 scale per 128 channels, the value of a code
+ * being decode(code) * scale, as for the output of ep_dispatch_fp8.
+ *     out[t, h] = bf16_rne( sum over j with dst_row[t,j] != -1 of
+ *                           topk_w[t,j] * decode(y_q[r, h]) * y_scale[r, h/128] )
+ * computed in fp32 as: c = fl32(topk_w[t,j] * y_scale[r, h/128]), then
+ * acc = fmaf(c, decode(y_q[r, h]), acc) in increasing j from +0, then one
+ * rounding to bf16 (decode is exact in fp32).  A token with no valid pair
+ * gives +0; a NaN code (0x7F, 0xFF) gives NaN.
+ *
+ *  y_q      [rows, H] uint8 e4m3 codes, 16-byte aligned.
+ *  y_scale  [rows, H/128] float32, row-major, 4-byte aligned.
+ *  topk_w   [T, k] float32;  dst_row [T, k] int32 as for ep_combine.
+ *  out      [T, H] bf16, 16-byte aligned.  H % 128 == 0.
+ */
+EP_API int ep_combine_fp8(const uint8_t* y_q, const float* y_scale, const float* topk_w,
+                          const int32_t* dst_row, int64_t T, int64_t H, int k, int64_t rows,
+                          void* out, uint32_t* status, void* stream);
+
+/*
  * Two-stage (rank, then expert) form of dispatch and combine -- the shape of
  * the pages' transport: one copy of a token per virtual rank it reaches,
  * expanded on arrival into that rank's experts (dispatch_copy_epilogue in the

@@ -68,6 +68,7 @@ def test_reference_arm_runs_on_cpu():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["host_cores"] == os.cpu_count()
 
 
 def test_reference_arm_under_torchrun_two_ranks():
@@ -110,3 +111,14 @@ def test_algorithmic_bytes_accounting():
     t2 = bench.algorithmic_bytes(wl, path="two_stage", rank_rows=nr)
     assert t2["dispatch"] == a["dispatch"] + 2 * nr * H * 2 + 2 * T * k * 4
     assert t2["combine"] == a["combine"] + 2 * nr * H * 2 + T * k * 8 + nr * 4
+    # FP8 expert outputs: codes plus a 4-byte scale per 128 channels in, bf16 out
+    c8 = bench.algorithmic_bytes(f, combine="fp8")
+    assert c8["combine"] == f.T * f.k * (f.H + f.H // 32) + f.T * f.H * 2 + f.T * f.k * 8
+    assert c8["dispatch"] == af["dispatch"]
+
+
+def test_host_cpu_record():
+    sys.path.insert(0, ROOT)
+    import bench
+    info = bench.host_cpu()
+    assert info["host_cores"] == os.cpu_count() and info["machine"]
