@@ -95,6 +95,18 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Lanes of the warp whose (valid) key equals this lane's: one ballot per key
+// bit.  Invalid lanes get an empty set and appear in no valid lane's set.
+__device__ __forceinline__ unsigned warp_peers(bool valid, int key, int key_bits) {
+    unsigned peers = __ballot_sync(kFullMask, valid);
+    for (int b = 0; b < key_bits; ++b) {
+        const bool bit = (key >> b) & 1;
+        const unsigned ones = __ballot_sync(kFullMask, bit);
+        peers &= bit ? ones : ~ones;
+    }
+    return valid ? peers : 0u;
+}
+
 // OR device-side condition bits into the optional status word: one atomic
 // per warp at most.
 __device__ __forceinline__ void warp_flag(uint32_t* status, bool cond, uint32_t bit) {
@@ -351,6 +363,32 @@ constexpr int kLayoutTokensPerChunk = kLayoutThreads;
 inline int64_t layout_num_chunks(int64_t T) {
     return (T + kLayoutTokensPerChunk - 1) / kLayoutTokensPerChunk;
 }
+
+// One-launch layouts (ep_layout_onelaunch.cu): a single block up to
+// EP_LAYOUT_BLOCK_MAX_TOKENS tokens, one 8-block cluster up to
+// EP_LAYOUT_CLUSTER_MAX_TOKENS (at most 2048); cudaErrorNotSupported (nothing
+// enqueued) when the shape does not fit their registers or shared memory.
+#ifndef EP_LAYOUT_BLOCK_MAX_TOKENS
+#define EP_LAYOUT_BLOCK_MAX_TOKENS 384
+#endif
+#ifndef EP_LAYOUT_CLUSTER_MAX_TOKENS
+#define EP_LAYOUT_CLUSTER_MAX_TOKENS 2048
+#endif
+#ifndef EP_LAYOUT_BLOCK_THREADS
+#define EP_LAYOUT_BLOCK_THREADS 1024
+#endif
+#ifndef EP_LAYOUT_CLUSTER_THREADS
+#define EP_LAYOUT_CLUSTER_THREADS 1024
+#endif
+cudaError_t launch_layout_block(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols,
+                                int R, int kind, int capacity, int align, int max_threads,
+                                int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+                                int32_t* rank_token_counts, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols,
+                                  int R, int kind, int capacity, int align, int max_threads,
+                                  int32_t* expert_counts, int32_t* expert_offsets,
+                                  int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
+                                  cudaStream_t stream);
 
 cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
                           int capacity, int align, int32_t* expert_counts, int32_t* expert_offsets,
