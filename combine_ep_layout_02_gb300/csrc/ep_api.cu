@@ -205,15 +205,18 @@ int layout_dispatch_checked(bool fp8, const int32_t* topk_idx, int64_t T, int k,
         rank_token_counts, fp8 ? static_cast<void*>(recv_q) : recv, recv_scale, rows, status,
         as_stream(stream));
     if (e != cudaErrorNotSupported) return cuda_status(e);
-    // outside the fused kernel's range: the two launches, same results
+    // outside the fused kernel's range: the layout, then the dispatch, which
+    // reads its first rows of x before waiting for the layout to finish (the
+    // layout kernel writes no x and lets it start only once all earlier work
+    // in the stream is complete); same results as the two calls
     rc = cuda_status(ep::launch_layout(topk_idx, T, k, E, R, kind, capacity, 1, expert_counts,
                                        expert_offsets, dst_row, rank_token_counts, status,
                                        static_cast<int32_t*>(workspace), as_stream(stream)));
     if (rc != EP_OK || T == 0) return rc;
     return cuda_status(fp8 ? ep::launch_dispatch_fp8(x, T, H, k, dst_row, recv_q, recv_scale,
-                                                     rows, status, as_stream(stream))
+                                                     rows, status, as_stream(stream), true)
                            : ep::launch_dispatch_bf16(x, T, H, k, dst_row, recv, rows, status,
-                                                      as_stream(stream)));
+                                                      as_stream(stream), true));
 }
 
 }  // namespace

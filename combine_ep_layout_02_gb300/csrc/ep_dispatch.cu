@@ -42,32 +42,47 @@ constexpr int kRowRegs = 8;        // destination rows held in registers per pas
 // 1257 us at 2 blocks per SM, 1245 us at one); 1-2 % slower at 1,024 to 2,048
 // tokens and no faster below, so smaller batches use the plain instance.  The
 // same change in the FP8 dispatch measured 0.15 % slower.
-template <int U, bool PREFETCH>
+//
+// EARLY: the first unit's first-pass loads are also issued before the wait on
+// the preceding kernel in the stream.  That is correct only when the
+// preceding kernel does not write x: ep_layout_dispatch launches this kernel
+// right behind its own layout kernel, which lets it start only after having
+// waited for all earlier work itself, so x is final by then.  The loads then
+// overlap the layout.
+template <int U, bool PREFETCH, bool EARLY>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k, int S,
                      int64_t slice, const int32_t* __restrict__ dst_row, uint4* __restrict__ recv,
                      int64_t rows, uint32_t* __restrict__ status) {
-    pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nunits = T * S;
     const int64_t stride = (int64_t)gridDim.x * kDispatchWarps;
-    for (int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5); g < nunits;
-         g += stride) {  // warp-uniform
+    const int64_t g0 = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
+    // the first pass's loads of unit g do not depend on the destination rows
+    uint4 first[U];
+    auto load_first = [&](int64_t g) {
+        const int64_t t = slice_row(g, S);
+        const int64_t vb = (g - t * S) * slice;
+        const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = vb + u * 32 + lane;
+            if (v < ve) first[u] = ld_stream_v4(x + t * nvec + v);
+        }
+    };
+    if (EARLY && g0 < nunits) load_first(g0);
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t g = g0; g < nunits; g += stride) {  // warp-uniform
         const int64_t t = slice_row(g, S);
         const int64_t vb = (g - t * S) * slice;  // this warp's column slice [vb, ve)
         const int64_t ve = vb + slice < nvec ? vb + slice : nvec;
         const uint4* src = x + t * nvec;
-        // the first pass's loads do not depend on the destination rows: issue
-        // them before the rows are read, so the two latencies overlap
-        uint4 first[U];
-        if (PREFETCH) {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = vb + u * 32 + lane;
-                if (v < ve) first[u] = ld_stream_v4(src + v);
-            }
-        }
+        // issue the first pass's loads before the rows are read, so the two
+        // latencies overlap
+        const bool early = EARLY && g == g0;  // warp-uniform
+        if (PREFETCH && !early) load_first(g);
+        const bool have_first = PREFETCH || early;
         const int my_row = load_dst_row(dst_row, t, k, rows, status);
         // k <= 8 is one pass; larger k re-reads the slice once per 8 destinations
         for (int j0 = 0; j0 < k; j0 += kRowRegs) {
@@ -79,7 +94,7 @@ dispatch_bf16_kernel(const uint4* __restrict__ x, int64_t T, int64_t nvec, int k
             }
             for (int64_t v0 = vb; v0 < ve; v0 += 32 * U) {
                 uint4 buf[U];
-                const bool pre = PREFETCH && j0 == 0 && v0 == vb;  // warp-uniform
+                const bool pre = have_first && j0 == 0 && v0 == vb;  // warp-uniform
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int64_t v = v0 + u * 32 + lane;
@@ -120,13 +135,15 @@ size_t dispatch_occupancy_smem() {
 
 cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
                                  const int32_t* dst_row, void* recv, int64_t rows,
-                                 uint32_t* status, cudaStream_t stream) {
+                                 uint32_t* status, cudaStream_t stream, bool early) {
     if (T == 0) return cudaSuccess;
     const int64_t nvec = H / 8;
     const RowSlices sl = row_slices(T, nvec);
     const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
     if (T < EP_DISPATCH_PREFETCH_MIN_TOKENS)
-        return launch_pdl(dispatch_bf16_kernel<EP_DISPATCH_U, false>, dim3(grid),
+        return launch_pdl(early ? dispatch_bf16_kernel<EP_DISPATCH_U, false, true>
+                                : dispatch_bf16_kernel<EP_DISPATCH_U, false, false>,
+                          dim3(grid),
                           dim3(kDispatchWarps * 32), 0, stream, static_cast<const uint4*>(x), T,
                           nvec, k, sl.S, sl.slice, dst_row, static_cast<uint4*>(recv), rows,
                           status);
@@ -138,7 +155,8 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
     // use).  A persistent grid of one block per SM looping over the tokens
     // (EP_DISPATCH_PERSISTENT=1) measured slower: 1408 us against 1263 us
     // with the same residency limit, 1422 us without it.
-    auto kern = dispatch_bf16_kernel<EP_DISPATCH_U, true>;
+    auto kern = early ? dispatch_bf16_kernel<EP_DISPATCH_U, true, true>
+                      : dispatch_bf16_kernel<EP_DISPATCH_U, true, false>;
     unsigned pgrid = grid;
 #if EP_DISPATCH_PERSISTENT
     {
@@ -149,8 +167,8 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
 #endif
     const size_t smem = dispatch_occupancy_smem();
     if (smem > 0) {
-        static std::atomic<uint64_t> configured{0};
-        const cudaError_t e = raise_smem_limit(kern, smem, configured);
+        static std::atomic<uint64_t> configured[2];
+        const cudaError_t e = raise_smem_limit(kern, smem, configured[early ? 1 : 0]);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(kern, dim3(pgrid), dim3(kDispatchWarps * 32), smem, stream,

@@ -35,25 +35,44 @@ constexpr int kRowRegs = 8;        // destination rows held in registers per pas
 // 16-byte store of codes per destination row; quantize16 in ep_internal.cuh);
 // 8 lanes form one 128-channel block; a warp covers 512 channels per group
 // and EP_FP8_U groups per iteration (their loads are issued together).
+//
+// EARLY: the first iteration's loads are issued before the wait on the
+// preceding kernel in the stream -- correct only when that kernel cannot
+// write x (ep_layout_dispatch: its own layout kernel, which lets this kernel
+// start only after having waited for all earlier work itself).
+template <bool EARLY>
 __global__ void EP_FP8_BOUNDS
 dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k, int S,
                     int64_t slice_ch, const int32_t* __restrict__ dst_row,
                     uint8_t* __restrict__ recv_q, float* __restrict__ recv_scale, int64_t rows,
                     uint32_t* __restrict__ status) {
     constexpr int U = EP_FP8_U;
-    pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * kDispatchWarps + (threadIdx.x >> 5);
     const int64_t t = slice_row(g, S);
-    if (t >= T) return;
     // this warp's channels [cb, ce): multiples of 512 (S > 1) or the whole row,
     // so that all 8 lanes of a 128-channel block agree on every bound below
     const int64_t cb = (g - t * S) * slice_ch;
     const int64_t ce = cb + slice_ch < H ? cb + slice_ch : H;
+    const uint16_t* src = x + t * H;
+    uint4 ea[U], eb[U];  // EARLY: the first iteration's loads
+    if (EARLY && t < T) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = cb + u * 512 + lane * 16;
+            ea[u] = make_uint4(0, 0, 0, 0);
+            eb[u] = make_uint4(0, 0, 0, 0);
+            if (c < ce) {
+                ea[u] = ld_stream_v4(src + c);
+                eb[u] = ld_stream_v4(src + c + 8);
+            }
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (t >= T) return;
     const int my_row = load_dst_row(dst_row, t, k, rows, status);
     const int64_t nblk = H / 128;
-    const uint16_t* src = x + t * H;
     for (int j0 = 0; j0 < k; j0 += kRowRegs) {
         int rr[kRowRegs];
 #pragma unroll
@@ -63,12 +82,16 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
         }
         for (int64_t c0 = cb; c0 < ce; c0 += 512 * U) {
             uint4 a[U], b[U];
+            const bool pre = EARLY && j0 == 0 && c0 == cb;  // warp-uniform
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t c = c0 + u * 512 + lane * 16;
                 a[u] = make_uint4(0, 0, 0, 0);
                 b[u] = make_uint4(0, 0, 0, 0);
-                if (c < ce) {  // H % 128 == 0: all 8 lanes of a block agree
+                if (pre) {
+                    a[u] = ea[u];
+                    b[u] = eb[u];
+                } else if (c < ce) {  // H % 128 == 0: all 8 lanes of a block agree
 #if EP_FP8_LOAD32
                     const Vec32 v = ld_stream_v8(src + c);  // 32-byte aligned: H % 128 == 0
                     a[u] = v.lo;
@@ -101,12 +124,13 @@ dispatch_fp8_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t H, int k,
 
 cudaError_t launch_dispatch_fp8(const void* x, int64_t T, int64_t H, int k,
                                 const int32_t* dst_row, uint8_t* recv_q, float* recv_scale,
-                                int64_t rows, uint32_t* status, cudaStream_t stream) {
+                                int64_t rows, uint32_t* status, cudaStream_t stream,
+                                bool early) {
     if (T == 0) return cudaSuccess;
     // slices in units of one lane's 16 channels (32 units = one 512-channel group)
     const RowSlices sl = row_slices(T, H / 16);
     const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
-    return launch_pdl(dispatch_fp8_kernel, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
+    return launch_pdl(early ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>, dim3(grid), dim3(kDispatchWarps * 32), 0, stream,
                       static_cast<const uint16_t*>(x), T, H, k, sl.S, sl.slice * 16, dst_row,
                       recv_q, recv_scale, rows, status);
 }

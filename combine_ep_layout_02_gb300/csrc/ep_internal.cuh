@@ -368,17 +368,27 @@ inline int64_t layout_num_chunks(int64_t T) {
 // EP_LAYOUT_BLOCK_MAX_TOKENS tokens, one 8-block cluster up to
 // EP_LAYOUT_CLUSTER_MAX_TOKENS (at most 2048); cudaErrorNotSupported (nothing
 // enqueued) when the shape does not fit their registers or shared memory.
+// Block sizes measured fastest (graph-replayed, E = 128 and 256): one block
+// of 256 threads up to 64 tokens (3.0 us; the cluster 3.4 us), clusters of
+// 256-thread blocks up to 768 tokens (128: 3.5 us; 512: 4.1 us) and of
+// 512-thread blocks above (2048: 6.1-6.4 us; 1024 threads: 6.4-6.7 us).
 #ifndef EP_LAYOUT_BLOCK_MAX_TOKENS
-#define EP_LAYOUT_BLOCK_MAX_TOKENS 384
+#define EP_LAYOUT_BLOCK_MAX_TOKENS 64
 #endif
 #ifndef EP_LAYOUT_CLUSTER_MAX_TOKENS
 #define EP_LAYOUT_CLUSTER_MAX_TOKENS 2048
 #endif
 #ifndef EP_LAYOUT_BLOCK_THREADS
-#define EP_LAYOUT_BLOCK_THREADS 1024
+#define EP_LAYOUT_BLOCK_THREADS 256
+#endif
+#ifndef EP_LAYOUT_CLUSTER_SMALL_MAX_TOKENS
+#define EP_LAYOUT_CLUSTER_SMALL_MAX_TOKENS 768
+#endif
+#ifndef EP_LAYOUT_CLUSTER_THREADS_SMALL
+#define EP_LAYOUT_CLUSTER_THREADS_SMALL 256
 #endif
 #ifndef EP_LAYOUT_CLUSTER_THREADS
-#define EP_LAYOUT_CLUSTER_THREADS 1024
+#define EP_LAYOUT_CLUSTER_THREADS 512
 #endif
 cudaError_t launch_layout_block(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols,
                                 int R, int kind, int capacity, int align, int max_threads,
@@ -404,13 +414,16 @@ cudaError_t launch_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, in
                                    float* recv_scale, int64_t rows, uint32_t* status,
                                    cudaStream_t stream);
 
+// `early`: the kernel may read x before waiting on the preceding kernel in
+// the stream (only when that kernel cannot write x; see ep_dispatch.cu).
 cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
                                  const int32_t* dst_row, void* recv, int64_t rows,
-                                 uint32_t* status, cudaStream_t stream);
+                                 uint32_t* status, cudaStream_t stream, bool early = false);
 
 cudaError_t launch_dispatch_fp8(const void* x, int64_t T, int64_t H, int k,
                                 const int32_t* dst_row, uint8_t* recv_q, float* recv_scale,
-                                int64_t rows, uint32_t* status, cudaStream_t stream);
+                                int64_t rows, uint32_t* status, cudaStream_t stream,
+                                bool early = false);
 
 cudaError_t launch_combine(const void* y, const float* topk_w, const int32_t* dst_row, int64_t T,
                            int64_t H, int k, int64_t rows, void* out, uint32_t* status,

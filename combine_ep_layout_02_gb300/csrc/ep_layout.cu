@@ -373,7 +373,10 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
     if (T <= EP_LAYOUT_CLUSTER_MAX_TOKENS) {
         const cudaError_t err =
             launch_layout_cluster(topk_idx, T, k, E, R_cols, R, kind, capacity, align,
-                                  EP_LAYOUT_CLUSTER_THREADS, expert_counts, expert_offsets,
+                                  T <= EP_LAYOUT_CLUSTER_SMALL_MAX_TOKENS
+                                      ? EP_LAYOUT_CLUSTER_THREADS_SMALL
+                                      : EP_LAYOUT_CLUSTER_THREADS,
+                                  expert_counts, expert_offsets,
                                   dst_row, rank_token_counts, status, stream);
         if (err != cudaErrorNotSupported) return err;
     }

@@ -73,7 +73,9 @@ struct OneLaunchSmem {
     int32_t* rc;         // [NW][R_cols]  per-warp tokens per virtual rank
     int32_t* off_local;  // [E]  exclusive scan of the padded totals within each 32-expert range
     int32_t* range_sum;  // [32] sum of the padded totals of each 32-expert range
-    int32_t* btot;       // [E + R_cols]  block totals, read by the other blocks (cluster)
+    uint32_t* wflags;    // [NW] condition flags each warp found among its ids
+    int32_t* btot;       // [E + R_cols + 1]  block totals and the block's flags, read by
+                         // the other blocks (cluster)
     int32_t* base;       // [E]  pairs of expert e in the cluster's earlier blocks (cluster)
 };
 
@@ -91,7 +93,7 @@ struct LanePairs {
 template <bool RANKS, int MAXP>
 __device__ __forceinline__ void warp_count_pieces(const int32_t* __restrict__ idx, int T, int k,
                                                   int E, int R_cols, int P, int p0, int np,
-                                                  RankOf rank_of, int rbits, int32_t* my_cnt,
+                                                  RankOf rank_of, int32_t* my_cnt,
                                                   int32_t* my_rc, LanePairs<MAXP>& lp,
                                                   uint32_t& flags) {
     const int lane = threadIdx.x & 31;
@@ -99,9 +101,6 @@ __device__ __forceinline__ void warp_count_pieces(const int32_t* __restrict__ id
     const int jl = lane - tl * k;
     const bool used = lane < P * k;
     const unsigned lt = lanemask_lt();
-    const int key_bits = bits_for(E);
-    // the lanes of this lane's token (for counting each rank once per token)
-    const unsigned grp = !used ? 0u : (k >= 32 ? kFullMask : ((1u << k) - 1u) << (tl * k));
 #pragma unroll
     for (int q = 0; q < MAXP; ++q) {
         const int t = (p0 + q) * P + tl;
@@ -118,17 +117,23 @@ __device__ __forceinline__ void warp_count_pieces(const int32_t* __restrict__ id
         const int e = lp.e[q];
         const bool valid = e >= 0 && e < E;
         if (e < -1 || e >= E) flags |= EP_FLAG_BAD_EXPERT;
-        const unsigned peers = warp_peers(valid, e, key_bits);
+        // lanes holding the same expert: every lane of the warp takes part in
+        // the match (invalid ids never equal a valid one, and invalid lanes
+        // drop their own set)
+        unsigned peers = __match_any_sync(kFullMask, e);
+        if (!valid) peers = 0u;
         if (valid) lp.lr[q] = my_cnt[e] + __popc(peers & lt);
         int r = 0;
         unsigned rpeers = 0;
         if (RANKS) {
+            // lanes of the same token reaching the same rank: each (token,
+            // rank) is counted by its first lane only
             r = valid ? rank_of(e) : 0;
-            rpeers = warp_peers(valid, r, rbits);
+            rpeers = __match_any_sync(kFullMask, valid ? (tl << 16) | r : (int)(0x80000000u | lane));
         }
         __syncwarp();
         if (valid && (__ffs(peers) - 1) == lane) my_cnt[e] += __popc(peers);
-        if (RANKS && valid && (rpeers & grp & lt) == 0) atomicAdd(&my_rc[r], 1);
+        if (RANKS && valid && (rpeers & lt) == 0) atomicAdd(&my_rc[r], 1);
         __syncwarp();
     }
 }
@@ -191,7 +196,8 @@ __device__ __forceinline__ int range_bases(const OneLaunchSmem& sm, int E, int& 
 
 // Phase 3: the rows of this lane's pairs.  base_e(e) adds the pairs of e in
 // earlier blocks (cluster) to the warp's prefix.  Rows go to g_dst (global,
-// if given) and s_dst (shared, if given); conditions become flag bits.
+// if given) and s_dst (shared, if given); a row at or past `rows` raises
+// EP_FLAG_BAD_ROW in `flags`.
 template <int MAXP, typename BaseFn>
 __device__ __forceinline__ void assign_pieces(const LanePairs<MAXP>& lp, int T, int k, int E, int kind,
                                               int capacity, int P, int p0, int np, int t_end,
@@ -213,13 +219,8 @@ __device__ __forceinline__ void assign_pieces(const LanePairs<MAXP>& lp, int T, 
         int dst = -1;
         if (valid) {
             const int slot = base_e(e) + my_cnt[e] + lp.lr[q];
-            if (kind == EP_LAYOUT_CONTIGUOUS) {
-                dst = rbase + sm.off_local[e] + slot;
-            } else if (slot < capacity) {
-                dst = e * capacity + slot;
-            } else {
-                flags |= EP_FLAG_OVERFLOW;
-            }
+            if (kind == EP_LAYOUT_CONTIGUOUS) dst = rbase + sm.off_local[e] + slot;
+            else if (slot < capacity) dst = e * capacity + slot;  // else overflow: -1
             if ((int64_t)dst >= rows) flags |= EP_FLAG_BAD_ROW;
         }
         if (used && t < t_end) {
@@ -237,18 +238,19 @@ struct NoBase {
 
 // The whole layout of T tokens by one block of NT threads; pieces of P
 // tokens, `ppw` per warp.  Outputs that are null are not written.  Returns
-// this lane's condition flags (BAD_ROW only against `rows`).  Two block
-// barriers; the block is synchronised on return only if `sync_end`.
+// the layout's condition flags (bad ids, masked overflow: an expert's count
+// above the capacity), the same in every thread; `row_flags` gets this
+// lane's EP_FLAG_BAD_ROW (a row at or past `rows`).  Two block barriers.
 template <int NT, bool RANKS>
 __device__ __forceinline__ uint32_t block_layout(const int32_t* __restrict__ idx, int T, int k,
                                                  int E, int R_cols, int kind, int capacity,
                                                  int align, int P, int ppw, RankOf rank_of,
-                                                 int rbits, const OneLaunchSmem& sm_in,
+                                                 const OneLaunchSmem& sm_in,
                                                  int32_t* __restrict__ expert_counts,
                                                  int32_t* __restrict__ expert_offsets,
                                                  int32_t* __restrict__ rank_token_counts,
                                                  int32_t* __restrict__ g_dst, int32_t* s_dst,
-                                                 int64_t rows) {
+                                                 int64_t rows, uint32_t& row_flags) {
     constexpr int NW = NT / 32;
     OneLaunchSmem sm = sm_in;
     const int warp = threadIdx.x >> 5;
@@ -259,16 +261,22 @@ __device__ __forceinline__ uint32_t block_layout(const int32_t* __restrict__ idx
     int32_t* my_cnt = sm.cnt + warp * E;
     uint32_t flags = 0;
     LanePairs<max_pieces<NT>()> lp;
-    warp_count_pieces<RANKS>(idx, T, k, E, R_cols, P, p0, np, rank_of, rbits, my_cnt,
+    warp_count_pieces<RANKS>(idx, T, k, E, R_cols, P, p0, np, rank_of, my_cnt,
                              sm.rc + warp * R_cols, lp, flags);
+    {
+        const unsigned wf = __reduce_or_sync(kFullMask, flags);
+        if (lane == 0) sm.wflags[warp] = wf;
+    }
     __syncthreads();
     // one thread per expert: prefix over warps, totals, 32-expert range scans
+    int ovf = 0;
     for (int e0 = 0; e0 < E; e0 += NT) {  // block-uniform
         const int e = e0 + threadIdx.x;
         int tt = 0;
         if (e < E) {
             const int c = expert_prefix_over_warps<NW>(sm.cnt, E, e);
             if (expert_counts) expert_counts[e] = c;
+            if (kind == EP_LAYOUT_MASKED && c > capacity) ovf = 1;
             tt = padded(c, align);
         }
         if (e0 + (threadIdx.x & ~31) < E) range_scan(tt, e, E, sm);  // warp-uniform
@@ -283,7 +291,9 @@ __device__ __forceinline__ uint32_t block_layout(const int32_t* __restrict__ idx
             if (rank_token_counts) rank_token_counts[r] = s;
         }
     }
-    __syncthreads();
+    uint32_t lflags = __syncthreads_or(ovf) ? EP_FLAG_OVERFLOW : 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) lflags |= sm.wflags[w];
     int rp;
     const int total = range_bases(sm, E, rp);
     if (expert_offsets) {
@@ -295,9 +305,8 @@ __device__ __forceinline__ uint32_t block_layout(const int32_t* __restrict__ idx
         if (threadIdx.x == 0) expert_offsets[E] = total;
     }
     assign_pieces(lp, T, k, E, kind, capacity, P, p0, np, T, sm, my_cnt, rp, rows, NoBase(),
-                  g_dst, s_dst, flags);
-    (void)lane;
-    return flags;
+                  g_dst, s_dst, row_flags);
+    return lflags;
 }
 
 // Carve the single-block arrays out of dynamic shared memory.
@@ -307,20 +316,21 @@ __device__ __forceinline__ OneLaunchSmem carve_block(int32_t* p, int NW, int E, 
     sm.rc = sm.cnt + NW * E;
     sm.off_local = sm.rc + NW * R_cols;
     sm.range_sum = sm.off_local + E;
+    sm.wflags = reinterpret_cast<uint32_t*>(sm.range_sum + 32);
     sm.btot = nullptr;
     sm.base = nullptr;
     return sm;
 }
 
 size_t block_smem_bytes(int NW, int E, int R_cols) {
-    return ((size_t)NW * (E + R_cols) + E + 32) * sizeof(int32_t);
+    return ((size_t)NW * (E + R_cols + 1) + E + 32) * sizeof(int32_t);
 }
 
 // Small batches: the whole layout in one block.
 template <int NT, bool RANKS>
 __global__ void __launch_bounds__(NT)
 layout_block_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
-                    int capacity, int align, int P, int ppw, RankOf rank_of, int rbits,
+                    int capacity, int align, int P, int ppw, RankOf rank_of,
                     int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_offsets,
                     int32_t* __restrict__ dst_row, int32_t* __restrict__ rank_token_counts,
                     uint32_t* __restrict__ status) {
@@ -328,13 +338,12 @@ layout_block_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     const OneLaunchSmem sm = carve_block(smem_i, NT / 32, E, R_cols);
     pdl_wait();
     pdl_trigger();
-    if (threadIdx.x == 0 && status) *status = 0u;  // ordered before the flags by the barriers
+    uint32_t row_flags = 0;  // no row limit here
     const uint32_t f = block_layout<NT, RANKS>(idx, T, k, E, R_cols, kind, capacity, align, P, ppw,
-                                               rank_of, rbits, sm, expert_counts, expert_offsets,
+                                               rank_of, sm, expert_counts, expert_offsets,
                                                rank_token_counts, dst_row, nullptr,
-                                               (int64_t)1 << 40);
-    const unsigned any = __reduce_or_sync(kFullMask, f);
-    if (any && status && (threadIdx.x & 31) == 0) atomicOr(status, any);
+                                               (int64_t)1 << 40, row_flags);
+    if (threadIdx.x == 0 && status) *status = f;  // the one write of the status word
 }
 
 // Medium batches: ONE launch of one 8-block cluster; block b owns tokens
@@ -349,7 +358,7 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 template <int NT, bool RANKS>
 __global__ void __launch_bounds__(NT)
 layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
-                      int capacity, int align, int P, int ppw, int tpb, RankOf rank_of, int rbits,
+                      int capacity, int align, int P, int ppw, int tpb, RankOf rank_of,
                       int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_offsets,
                       int32_t* __restrict__ dst_row, int32_t* __restrict__ rank_token_counts,
                       uint32_t* __restrict__ status) {
@@ -358,8 +367,8 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
     cg::cluster_group cluster = cg::this_cluster();
     const int b = (int)cluster.block_rank();
     OneLaunchSmem sm = carve_block(smem_i, NW, E, R_cols);
-    sm.btot = sm.range_sum + 32;       // [E + R_cols]
-    sm.base = sm.btot + E + R_cols;    // [E]
+    sm.btot = reinterpret_cast<int32_t*>(sm.wflags + NW);  // [E + R_cols + 1]
+    sm.base = sm.btot + E + R_cols + 1;                     // [E]
     const int warp = threadIdx.x >> 5;
     const int t0 = b * tpb;
     const int tb = T - t0 < 0 ? 0 : (T - t0 < tpb ? T - t0 : tpb);  // this block's tokens
@@ -370,12 +379,15 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
 
     pdl_wait();
     pdl_trigger();
-    if (b == 0 && threadIdx.x == 0 && status) *status = 0u;  // ordered by the cluster barrier
     int32_t* my_cnt = sm.cnt + warp * E;
     uint32_t flags = 0;
     LanePairs<max_pieces<NT>()> lp;
-    warp_count_pieces<RANKS>(bidx, tb, k, E, R_cols, P, p0, np, rank_of, rbits, my_cnt,
+    warp_count_pieces<RANKS>(bidx, tb, k, E, R_cols, P, p0, np, rank_of, my_cnt,
                              sm.rc + warp * R_cols, lp, flags);
+    {
+        const unsigned wf = __reduce_or_sync(kFullMask, flags);
+        if ((threadIdx.x & 31) == 0) sm.wflags[warp] = wf;
+    }
     __syncthreads();
     // block totals (prefix over this block's warps kept in cnt)
     for (int e = threadIdx.x; e < E; e += NT) sm.btot[e] = expert_prefix_over_warps<NW>(sm.cnt, E, e);
@@ -386,9 +398,16 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
             for (int w = 0; w < NW; ++w) s += sm.rc[w * R_cols + r];
             sm.btot[E + r] = s;
         }
+    if (threadIdx.x == 0) {  // the block's flags, for block 0
+        uint32_t bf = 0;
+        for (int w = 0; w < NW; ++w) bf |= sm.wflags[w];
+        sm.btot[E + R_cols] = (int32_t)bf;
+    }
     cluster.sync();  // every block's totals are complete and visible
     // one thread per expert: pairs in earlier blocks and the cluster total,
-    // read from the 8 blocks' shared memory
+    // read from the 8 blocks' shared memory; masked overflow is a total above
+    // the capacity
+    int ovf = 0;
     for (int e0 = 0; e0 < E; e0 += NT) {  // block-uniform
         const int e = e0 + threadIdx.x;
         int tt = 0;
@@ -404,6 +423,7 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
             }
             sm.base[e] = before;
             if (b == 0) expert_counts[e] = total;
+            if (kind == EP_LAYOUT_MASKED && total > capacity) ovf = 1;
             tt = padded(total, align);
         }
         if (e0 + (threadIdx.x & ~31) < E) range_scan(tt, e, E, sm);  // warp-uniform
@@ -417,8 +437,12 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
             rank_token_counts[r] = s;
         }
     }
+    uint32_t cflags = 0;  // block 0: every block's flags
+    if (b == 0 && threadIdx.x == 0)
+        for (int q = 0; q < kClusterBlocks; ++q)
+            cflags |= (uint32_t)cluster.map_shared_rank(sm.btot, q)[E + R_cols];
     cluster_arrive_release();  // this block's remote reads are done
-    __syncthreads();
+    if (__syncthreads_or(ovf)) cflags |= EP_FLAG_OVERFLOW;
     int rp;
     const int total = range_bases(sm, E, rp);
     if (b == 0) {
@@ -430,15 +454,16 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
         if (threadIdx.x == 0) expert_offsets[E] = total;
     }
     const int32_t* base = sm.base;
+    uint32_t row_flags = 0;  // no row limit here
     assign_pieces(lp, tb, k, E, kind, capacity, P, p0, np, tb, sm, my_cnt, rp, (int64_t)1 << 40,
-                  [base](int e) { return base[e]; }, dst_row + (int64_t)t0 * k, nullptr, flags);
-    const unsigned any = __reduce_or_sync(kFullMask, flags);
-    if (any && status && (threadIdx.x & 31) == 0) atomicOr(status, any);
+                  [base](int e) { return base[e]; }, dst_row + (int64_t)t0 * k, nullptr,
+                  row_flags);
+    if (b == 0 && threadIdx.x == 0 && status) *status = cflags;  // the one write of the status word
     cluster_wait_acquire();  // no block leaves while another may still read its totals
 }
 
 size_t cluster_smem_bytes(int NW, int E, int R_cols) {
-    return block_smem_bytes(NW, E, R_cols) + ((size_t)2 * E + R_cols) * sizeof(int32_t);
+    return block_smem_bytes(NW, E, R_cols) + ((size_t)2 * E + R_cols + 1) * sizeof(int32_t);
 }
 
 // Pieces per warp for `tokens` tokens over NW warps (pieces of P = 32/k tokens).
@@ -455,20 +480,20 @@ cudaError_t prepare(K kernel, size_t smem, std::atomic<uint64_t>& configured) {
 
 template <int NT, bool RANKS>
 cudaError_t launch_block_nt(const int32_t* idx, int T, int k, int E, int R_cols, int kind,
-                            int capacity, int align, int ppw, RankOf rof, int rbits,
+                            int capacity, int align, int ppw, RankOf rof,
                             int32_t* counts, int32_t* offsets, int32_t* dst_row, int32_t* rtc,
                             uint32_t* status, size_t smem, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};
     cudaError_t err = prepare(layout_block_kernel<NT, RANKS>, smem, configured);
     if (err != cudaSuccess) return err;
     return launch_pdl(layout_block_kernel<NT, RANKS>, dim3(1), dim3(NT), smem, stream, idx, T, k,
-                      E, R_cols, kind, capacity, align, 32 / k, ppw, rof, rbits, counts, offsets,
+                      E, R_cols, kind, capacity, align, 32 / k, ppw, rof, counts, offsets,
                       dst_row, rtc, status);
 }
 
 template <int NT, bool RANKS>
 cudaError_t launch_cluster_nt(const int32_t* idx, int T, int k, int E, int R_cols, int kind,
-                              int capacity, int align, int ppw, int tpb, RankOf rof, int rbits,
+                              int capacity, int align, int ppw, int tpb, RankOf rof,
                               int32_t* counts, int32_t* offsets, int32_t* dst_row, int32_t* rtc,
                               uint32_t* status, size_t smem, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};
@@ -490,7 +515,7 @@ cudaError_t launch_cluster_nt(const int32_t* idx, int T, int k, int E, int R_col
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, idx, T, k, E, R_cols, kind, capacity, align, 32 / k, ppw,
-                              tpb, rof, rbits, counts, offsets, dst_row, rtc, status);
+                              tpb, rof, counts, offsets, dst_row, rtc, status);
 }
 
 // ---- layout fused with dispatch (few tokens) --------------------------------
@@ -508,7 +533,7 @@ constexpr int kLDMaxTokens = 128;  // above, the two launches measured faster (2
 template <bool FP8, bool RANKS>
 __global__ void __launch_bounds__(kLDThreads)
 layout_dispatch_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
-                       int capacity, int P, int ppw, RankOf rank_of, int rbits,
+                       int capacity, int P, int ppw, RankOf rank_of,
                        const uint16_t* __restrict__ x, int64_t H, int S, int64_t slice,
                        int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_offsets,
                        int32_t* __restrict__ dst_row, int32_t* __restrict__ rank_token_counts,
@@ -554,15 +579,16 @@ layout_dispatch_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int
     }
 
     // ---- the layout, as layout_block_kernel, into shared memory
-    if (threadIdx.x == 0) s_flags = 0u;
+    if (threadIdx.x == 0) s_flags = 0u;  // ordered before the atomics by block_layout's barriers
+    uint32_t row_flags = 0;
     const uint32_t f = block_layout<NT, RANKS>(
-        idx, T, k, E, R_cols, kind, capacity, 1, P, ppw, rank_of, rbits, sm,
+        idx, T, k, E, R_cols, kind, capacity, 1, P, ppw, rank_of, sm,
         lead ? expert_counts : nullptr, lead ? expert_offsets : nullptr,
-        lead ? rank_token_counts : nullptr, lead ? dst_row : nullptr, s_dst, rows);
-    const unsigned any = __reduce_or_sync(kFullMask, f);
+        lead ? rank_token_counts : nullptr, lead ? dst_row : nullptr, s_dst, rows, row_flags);
+    const unsigned any = __reduce_or_sync(kFullMask, row_flags);
     if (any && lane == 0) atomicOr(&s_flags, any);
     __syncthreads();  // s_dst and s_flags complete
-    if (lead && threadIdx.x == 0 && status) *status = s_flags;
+    if (lead && threadIdx.x == 0 && status) *status = s_flags | f;
     if (!has_unit) return;
 
     // ---- dispatch of this warp's unit from the shared layout
@@ -635,7 +661,7 @@ size_t layout_dispatch_smem_bytes(int T, int k, int E, int R_cols) {
 
 template <bool FP8, bool RANKS>
 cudaError_t launch_ld(const int32_t* topk_idx, int T, int k, int E, int R_cols, int kind,
-                      int capacity, int ppw, RankOf rof, int rbits, const void* x, int64_t H,
+                      int capacity, int ppw, RankOf rof, const void* x, int64_t H,
                       RowSlices sl, unsigned grid, int32_t* counts, int32_t* offsets,
                       int32_t* dst_row, int32_t* rtc, void* recv, float* recv_scale,
                       int64_t rows, uint32_t* status, size_t smem, cudaStream_t stream) {
@@ -644,7 +670,7 @@ cudaError_t launch_ld(const int32_t* topk_idx, int T, int k, int E, int R_cols, 
     cudaError_t err = prepare(kern, smem, configured);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(grid), dim3(kLDThreads), smem, stream, topk_idx, T, k, E, R_cols,
-                      kind, capacity, 32 / k, ppw, rof, rbits, static_cast<const uint16_t*>(x), H,
+                      kind, capacity, 32 / k, ppw, rof, static_cast<const uint16_t*>(x), H,
                       sl.S, sl.slice, counts, offsets, dst_row, rtc, recv, recv_scale, rows,
                       status);
 }
@@ -663,11 +689,10 @@ cudaError_t launch_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, in
     const size_t smem = layout_dispatch_smem_bytes((int)T, k, E, R_cols);
     if (ppw > max_pieces<kLDThreads>() || smem > kSmemLimit) return cudaErrorNotSupported;
     const RankOf rof = make_rank_of(E, R);
-    const int rbits = bits_for(R_cols > 0 ? R_cols : 1);
     const RowSlices sl = row_slices(T, fp8 ? H / 16 : H / 8);
     const unsigned grid = (unsigned)((T * sl.S + kLDWarps - 1) / kLDWarps);
 #define EP_LD_ARGS                                                                             \
-    topk_idx, (int)T, k, E, R_cols, kind, capacity, ppw, rof, rbits, x, H, sl, grid,           \
+    topk_idx, (int)T, k, E, R_cols, kind, capacity, ppw, rof, x, H, sl, grid,           \
         expert_counts, expert_offsets, dst_row, rank_token_counts, recv, recv_scale, rows, status, \
         smem, stream
     if (fp8)
@@ -683,8 +708,7 @@ cudaError_t launch_layout_block(const int32_t* topk_idx, int64_t T, int k, int E
                                 cudaStream_t stream) {
     if (T < 1 || T > kClusterMaxTokens) return cudaErrorNotSupported;
     const RankOf rof = make_rank_of(E, R);
-    const int rbits = bits_for(R_cols > 0 ? R_cols : 1);
-    for (int nt = max_threads; nt >= 128; nt /= 2) {
+    for (int nt = max_threads; nt >= 32; nt /= 2) {
         const int NW = nt / 32;
         const int ppw = pieces_per_warp(T, k, NW);
         const size_t smem = block_smem_bytes(NW, E, R_cols);
@@ -694,11 +718,11 @@ cudaError_t launch_layout_block(const int32_t* topk_idx, int64_t T, int k, int E
     case N:                                                                                      \
         return R_cols > 0                                                                        \
                    ? launch_block_nt<N, true>(topk_idx, (int)T, k, E, R_cols, kind, capacity,    \
-                                              align, ppw, rof, rbits, expert_counts,             \
+                                              align, ppw, rof, expert_counts,             \
                                               expert_offsets, dst_row, rank_token_counts,        \
                                               status, smem, stream)                              \
                    : launch_block_nt<N, false>(topk_idx, (int)T, k, E, R_cols, kind, capacity,   \
-                                               align, ppw, rof, rbits, expert_counts,            \
+                                               align, ppw, rof, expert_counts,            \
                                                expert_offsets, dst_row, rank_token_counts,       \
                                                status, smem, stream);
         switch (nt) {
@@ -706,6 +730,8 @@ cudaError_t launch_layout_block(const int32_t* topk_idx, int64_t T, int k, int E
             EP_BLOCK_CASE(512)
             EP_BLOCK_CASE(256)
             EP_BLOCK_CASE(128)
+            EP_BLOCK_CASE(64)
+            EP_BLOCK_CASE(32)
             default: break;
         }
 #undef EP_BLOCK_CASE
@@ -720,9 +746,8 @@ cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int
                                   cudaStream_t stream) {
     if (T < 1 || T > kClusterMaxTokens) return cudaErrorNotSupported;
     const RankOf rof = make_rank_of(E, R);
-    const int rbits = bits_for(R_cols > 0 ? R_cols : 1);
     const int tpb = (int)((T + kClusterBlocks - 1) / kClusterBlocks);
-    for (int nt = max_threads; nt >= 128; nt /= 2) {
+    for (int nt = max_threads; nt >= 32; nt /= 2) {
         const int NW = nt / 32;
         const int ppw = pieces_per_warp(tpb, k, NW);
         const size_t smem = cluster_smem_bytes(NW, E, R_cols);
@@ -732,11 +757,11 @@ cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int
     case N:                                                                                      \
         return R_cols > 0                                                                        \
                    ? launch_cluster_nt<N, true>(topk_idx, (int)T, k, E, R_cols, kind, capacity,  \
-                                                align, ppw, tpb, rof, rbits, expert_counts,      \
+                                                align, ppw, tpb, rof, expert_counts,      \
                                                 expert_offsets, dst_row, rank_token_counts,      \
                                                 status, smem, stream)                            \
                    : launch_cluster_nt<N, false>(topk_idx, (int)T, k, E, R_cols, kind,           \
-                                                 capacity, align, ppw, tpb, rof, rbits,          \
+                                                 capacity, align, ppw, tpb, rof,          \
                                                  expert_counts, expert_offsets, dst_row,         \
                                                  rank_token_counts, status, smem, stream);
         switch (nt) {
@@ -744,6 +769,8 @@ cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int
             EP_CLUSTER_CASE(512)
             EP_CLUSTER_CASE(256)
             EP_CLUSTER_CASE(128)
+            EP_CLUSTER_CASE(64)
+            EP_CLUSTER_CASE(32)
             default: break;
         }
 #undef EP_CLUSTER_CASE

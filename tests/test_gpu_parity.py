@@ -519,6 +519,13 @@ def test_dispatch_fp8_every_pattern_at_fixed_scales():
     (100, 8, 64, 4, "contiguous", 0, 512, False, 7, False),        # rows too few: BAD_ROW
     (257, 8, 256, 16, "contiguous", 0, 1024, True, 0, False),      # above the fused range
     (3000, 8, 256, 16, "masked", 3000, 512, False, 0, False),
+    # two launches, the dispatch reading x before the layout ends: the
+    # decode-like FP8 shape, the masked BF16 shape, and the large-batch
+    # instance (one block per SM) from 16,384 tokens
+    (2048, 8, 256, 16, "masked", 2048, 7168, True, 0, False),
+    (2048, 8, 128, 4, "masked", 2048, 2048, False, 0, True),
+    (17000, 8, 256, 16, "contiguous", 0, 512, False, 0, False),
+    (17000, 8, 256, 16, "contiguous", 0, 512, True, 0, False),
 ])
 def test_layout_dispatch_matches_oracle(T, k, E, R, kind, cap, H, fp8, rows_cut, bad):
     rng = np.random.default_rng(T * 31 + H + k)
