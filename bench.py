@@ -172,19 +172,31 @@ def source_hash(rel):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel (else None)."""
+def ncu_traffic(kernel, wl):
+    """DRAM bytes per launch of `kernel` on workload `wl`, from the committed
+    ncu capture (profiles/traffic.json), or None.  Captures are taken on a
+    smaller case of the same shape (same H and k, fewer tokens) and scaled
+    by the token count: a launch's reads and writes are per-token rows.  Only
+    used while the kernel's source is the one the capture was taken on."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             tab = json.load(f)
     except (OSError, ValueError):
         return None
-    ent = tab.get(workload, {}).get(kernel)
-    if not ent or ent.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+    ent = tab.get("kernels", {}).get(kernel)
+    if not ent or kernel not in KERNEL_SOURCES:
         return None
-    return ent.get("dram_bytes_per_launch")
+    if ent.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    if ent.get("H") != wl.H or ent.get("k") != wl.k or not ent.get("tokens"):
+        return None
+    lo, hi = ent.get("valid_tokens", [0, 1 << 62])  # the token range that runs the captured instance
+    if not lo <= wl.T <= hi:
+        return None
+    per_launch = ent["dram_bytes_read"] + ent["dram_bytes_write"]
+    return {"bytes": per_launch * wl.T / ent["tokens"], "captured_tokens": ent["tokens"],
+            "captured_workload": ent.get("workload"), "scale": wl.T / ent["tokens"]}
 
 
 def algorithmic_bytes(wl, path="direct", fused=False, rank_rows=0, combine="bf16"):
@@ -687,10 +699,13 @@ def run_ours(args, rank, world, local):
                 "frac": frac, "peak_source": peak_src + " (%s)" % (
                     "MEASURED_PEAKS.json hbm_gbs" if peak_src == "measured" else "6.8 TB/s"),
                 "algorithmic_bytes_per_launch": alg[dominant],
-                # counters were captured on the full-size workload only
-                "traffic": None if (args.tokens or args.seed is not None or args.path != "direct"
-                                    or args.fused)
-                else ncu_traffic(kname, wl.name)}
+                "traffic": None}
+    tr = None if (args.path != "direct" or args.fused) else ncu_traffic(kname, wl)
+    if tr is not None:
+        roofline["traffic"] = tr["bytes"]
+        roofline["traffic_note"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch "
+                                    "at %d tokens (%s), scaled x%.3g by the token count" % (
+                                        tr["captured_tokens"], tr["captured_workload"], tr["scale"]))
     kernels = {}
     step_sum = sum(per_launch_ms.values())
     for n in per_launch_ms:

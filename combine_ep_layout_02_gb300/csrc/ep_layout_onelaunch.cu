@@ -9,7 +9,8 @@
 // tokens, one pair per lane (lane l: token l / k of the piece, j = l % k), and
 // give each warp a contiguous run of pieces.  Per piece a warp ranks equal
 // experts with popc(peers & lanemask_lt), the peers coming from one ballot
-// per bit of the expert id, and keeps a running per-warp count of each expert
+// per bit of the expert id (match.any, one instruction, measured slower from
+// a few pieces per warp on: 2,048 tokens 6.9 -> 7.8 us), and keeps a running per-warp count of each expert
 // in its own shared-memory row -- no block barrier until every warp has
 // counted.  The ids stay in registers.  Then:
 //   single block (layout_block_kernel): one thread per expert turns the warps'
@@ -37,6 +38,14 @@ namespace cg = cooperative_groups;
 // a thread), 16 in smaller ones.
 template <int NT>
 __host__ __device__ constexpr int max_pieces() { return NT >= 1024 ? 8 : 16; }
+// The per-piece loops are not unrolled: each pass is the same code, fetched
+// once into the instruction cache (instruction fetch was the top stall of
+// the unrolled form, whose every piece was new code; 128 tokens 4.64 ->
+// 4.30 us); the pieces' ids and slots then live in local memory.
+#ifndef EP_LAYOUT_PIECE_UNROLL
+#define EP_LAYOUT_PIECE_UNROLL 1
+#endif
+constexpr int kPieceUnroll = EP_LAYOUT_PIECE_UNROLL;
 constexpr int kClusterBlocks = 8;
 constexpr int kClusterMaxTokens = 2048;
 constexpr size_t kSmemLimit = 160 * 1024;
@@ -101,6 +110,10 @@ __device__ __forceinline__ void warp_count_pieces(const int32_t* __restrict__ id
     const int jl = lane - tl * k;
     const bool used = lane < P * k;
     const unsigned lt = lanemask_lt();
+    const int key_bits = bits_for(E);
+    const int rbits = bits_for(R_cols > 0 ? R_cols : 1);
+    // the lanes of this lane's token (for counting each rank once per token)
+    const unsigned grp = !used ? 0u : (k >= 32 ? kFullMask : ((1u << k) - 1u) << (tl * k));
 #pragma unroll
     for (int q = 0; q < MAXP; ++q) {
         const int t = (p0 + q) * P + tl;
@@ -111,29 +124,23 @@ __device__ __forceinline__ void warp_count_pieces(const int32_t* __restrict__ id
     if (RANKS)
         for (int i = lane; i < R_cols; i += 32) my_rc[i] = 0;
     __syncwarp();
-#pragma unroll
+#pragma unroll kPieceUnroll
     for (int q = 0; q < MAXP; ++q) {
         if (q >= np) break;  // warp-uniform
         const int e = lp.e[q];
         const bool valid = e >= 0 && e < E;
         if (e < -1 || e >= E) flags |= EP_FLAG_BAD_EXPERT;
-        // lanes holding the same expert: every lane of the warp takes part in
-        // the match (invalid ids never equal a valid one, and invalid lanes
-        // drop their own set)
-        unsigned peers = __match_any_sync(kFullMask, e);
-        if (!valid) peers = 0u;
+        const unsigned peers = warp_peers(valid, e, key_bits);
         if (valid) lp.lr[q] = my_cnt[e] + __popc(peers & lt);
         int r = 0;
         unsigned rpeers = 0;
         if (RANKS) {
-            // lanes of the same token reaching the same rank: each (token,
-            // rank) is counted by its first lane only
             r = valid ? rank_of(e) : 0;
-            rpeers = __match_any_sync(kFullMask, valid ? (tl << 16) | r : (int)(0x80000000u | lane));
+            rpeers = warp_peers(valid, r, rbits) & grp;  // same token, same rank
         }
         __syncwarp();
         if (valid && (__ffs(peers) - 1) == lane) my_cnt[e] += __popc(peers);
-        if (RANKS && valid && (rpeers & lt) == 0) atomicAdd(&my_rc[r], 1);
+        if (RANKS && valid && (rpeers & lt) == 0) atomicAdd(&my_rc[r], 1);  // first of the token
         __syncwarp();
     }
 }
@@ -209,7 +216,7 @@ __device__ __forceinline__ void assign_pieces(const LanePairs<MAXP>& lp, int T, 
     const int tl = lane / k;
     const int jl = lane - tl * k;
     const bool used = lane < P * k;
-#pragma unroll
+#pragma unroll kPieceUnroll
     for (int q = 0; q < MAXP; ++q) {
         if (q >= np) break;  // warp-uniform
         const int e = lp.e[q];
