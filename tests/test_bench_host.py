@@ -122,3 +122,24 @@ def test_host_cpu_record():
     import bench
     info = bench.host_cpu()
     assert info["host_cores"] == os.cpu_count() and info["machine"]
+
+
+def test_ncu_traffic_scales_by_tokens(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    from combine_ep_layout_02_gb300 import workloads as W
+    os.makedirs(tmp_path / "profiles")
+    ent = {"kernel": "k", "workload": "prefill", "tokens": 16384, "H": 7168, "k": 8,
+           "valid_tokens": [16384, 1 << 40], "dram_bytes_read": 100, "dram_bytes_write": 300,
+           "source_sha256_16": "abc"}
+    with open(tmp_path / "profiles" / "traffic.json", "w") as f:
+        json.dump({"kernels": {"dispatch": ent}}, f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda rel: "abc")
+    tr = bench.ncu_traffic("dispatch", W.WORKLOADS["prefill"])
+    assert tr["bytes"] == 400 * 4 and tr["scale"] == 4          # 65,536 / 16,384 tokens
+    assert bench.ncu_traffic("dispatch", W.WORKLOADS["prefill"].scaled(T=8192)) is None  # other instance
+    assert bench.ncu_traffic("dispatch", W.WORKLOADS["masked"]) is None                  # other H
+    assert bench.ncu_traffic("combine", W.WORKLOADS["prefill"]) is None                  # not captured
+    monkeypatch.setattr(bench, "source_hash", lambda rel: "changed")
+    assert bench.ncu_traffic("dispatch", W.WORKLOADS["prefill"]) is None                 # source changed
