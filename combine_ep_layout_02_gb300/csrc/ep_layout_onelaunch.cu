@@ -9,10 +9,10 @@
 // tokens, one pair per lane (lane l: token l / k of the piece, j = l % k), and
 // give each warp a contiguous run of pieces.  Per piece a warp ranks equal
 // experts with popc(peers & lanemask_lt), the peers coming from one ballot
-// per bit of the expert id (match.any, one instruction, measured slower from
-// a few pieces per warp on: 2,048 tokens 6.9 -> 7.8 us), and keeps a running per-warp count of each expert
-// in its own shared-memory row -- no block barrier until every warp has
-// counted.  The ids stay in registers.  Then:
+// per bit of the expert id, and keeps a running per-warp count of each
+// expert in its own shared-memory row -- no block barrier until every warp
+// has counted.  (match.any gives the peers in one instruction but runs on a
+// shared per-SM unit: 2,048 tokens 6.9 -> 7.8 us.)  Then:
 //   single block (layout_block_kernel): one thread per expert turns the warps'
 //     counts into their exclusive prefix over warps and the expert's total;
 //     each warp scans its 32 experts' (padded) totals; after the second
@@ -23,8 +23,10 @@
 //     cluster barrier; the blocks then only signal that their remote reads
 //     are done and wait for the others' signals just before exiting, so the
 //     slot assignment overlaps that second cluster barrier.
-// The slot of a pair is the number of earlier pairs (flattened t*k + j) with
-// the same expert, as in the chunked kernels of ep_layout.cu.
+// The status word is written once, by one thread: bad ids are collected per
+// warp and the masked overflow is read off the expert totals.  The slot of a
+// pair is the number of earlier pairs (flattened t*k + j) with the same
+// expert, as in the chunked kernels of ep_layout.cu.
 #include <cooperative_groups.h>
 
 #include "ep_internal.cuh"
@@ -34,8 +36,8 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-// Pieces per warp held in registers: 8 in 1024-thread blocks (64 registers
-// a thread), 16 in smaller ones.
+// Pieces per warp a lane keeps (ids and slots): 8 in 1024-thread blocks
+// (64 registers a thread), 16 in smaller ones.
 template <int NT>
 __host__ __device__ constexpr int max_pieces() { return NT >= 1024 ? 8 : 16; }
 // The per-piece loops are not unrolled: each pass is the same code, fetched

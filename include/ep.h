@@ -235,8 +235,11 @@ EP_API int ep_dispatch_fp8(const void* x, int64_t T, int64_t H, int k, const int
  * (counts, offsets, dst_row, rank_token_counts, recv, status) are identical
  * to the two calls made in sequence.  Up to 128 tokens this is one kernel
  * launch: every block computes the whole layout in shared memory and
- * dispatches its share of the rows; larger batches run the two launches.
- * The workspace rules of ep_layout apply.
+ * dispatches its share of the rows.  Larger batches run the two launches,
+ * the dispatch issuing its first loads of x while the layout still runs
+ * (x must therefore not be written by earlier work that is still running on
+ * another stream without an event between them -- as for any input).  The
+ * workspace rules of ep_layout apply.
  */
 EP_API int ep_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, int E, int R, int kind,
                               int capacity, const void* x, int64_t H, int32_t* expert_counts,

@@ -125,6 +125,20 @@ def test_dispatch_combine_argument_validation(lib):
     assert lib.ep_status_read(None, None, None) == 1
 
 
+def test_combine_fp8_argument_validation(lib):
+    # (y_q, y_scale, topk_w, dst_row, T, H, k, rows, out, status, stream)
+    assert lib.ep_combine_fp8(FAKE, FAKE, FAKE, FAKE, 4, 64, 8, 32, FAKE, None, None) == 2    # H % 128
+    assert lib.ep_combine_fp8(FAKE, FAKE, FAKE, FAKE, 4, 256, 0, 32, FAKE, None, None) == 1   # k
+    assert lib.ep_combine_fp8(FAKE, FAKE, FAKE, FAKE, 4, 256, 8, 32, None, None, None) == 1   # out NULL
+    assert lib.ep_combine_fp8(None, FAKE, FAKE, FAKE, 4, 256, 8, 32, FAKE, None, None) == 1   # codes NULL
+    assert lib.ep_combine_fp8(FAKE, None, FAKE, FAKE, 4, 256, 8, 32, FAKE, None, None) == 1   # scales NULL
+    assert lib.ep_combine_fp8(ctypes.c_void_p((1 << 20) + 8), FAKE, FAKE, FAKE, 4, 256, 8, 32, FAKE,
+                              None, None) == 2                                                 # codes not 16-B aligned
+    assert lib.ep_combine_fp8(FAKE, ctypes.c_void_p((1 << 20) + 2), FAKE, FAKE, 4, 256, 8, 32, FAKE,
+                              None, None) == 2                                                 # scales not 4-B aligned
+    assert lib.ep_combine_fp8(FAKE, FAKE, FAKE, FAKE, 0, 256, 8, 32, FAKE, None, None) == 0   # T == 0: no-op
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     from combine_ep_layout_02_gb300 import binding
     monkeypatch.setattr(binding, "_lib", None)

@@ -64,8 +64,11 @@ def test_no_writes_outside_outputs(T, kind):
     y = torch.randn(rows, H, device=DEV).to(torch.bfloat16)
     gout = Guarded((T, H), torch.bfloat16)
     ep.combine(y, w, d, out=gout.t, status=lay.status)
+    y_q, y_s = W.fp8_expert_outputs(wl, device=DEV)
+    gout8 = Guarded((T, H), torch.bfloat16)
+    ep.combine_fp8(y_q, y_s, w, d, out=gout8.t, status=lay.status)
     assert ep.status_read(lay.status) & ep.EP_FLAG_BAD_ROW
-    guards += [grecv, gq, gs, gout]
+    guards += [grecv, gq, gs, gout, gout8]
     # two-stage path
     cap = ep.rank_rows_bound(T, k, R)
     gr = [Guarded((R,), torch.int32), Guarded((R + 1,), torch.int32), Guarded((T, k), torch.int32),
