@@ -9,5 +9,5 @@ from .binding import (  # noqa: F401
     EpError, LayoutOut, Pipeline, combine, combine_fp8, dispatch, dispatch_fp8, layout, layout_dispatch,
     layout_workspace_bytes, load,
     layout_static_ws, status_read, rank_layout, rank_rows_bound, expand, expand_fp8, combine_partial,
-    combine_reduce, RankLayoutOut, EP_FLAG_BAD_EXPERT, EP_FLAG_OVERFLOW, EP_FLAG_BAD_ROW,
+    combine_reduce, RankLayoutOut, EP_FLAG_BAD_EXPERT, EP_FLAG_OVERFLOW, EP_FLAG_BAD_ROW, EP_FLAG_TIMEOUT,
 )

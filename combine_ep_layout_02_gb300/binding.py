@@ -23,6 +23,7 @@ EP_ERR_CUDA = 4
 EP_FLAG_BAD_EXPERT = 1
 EP_FLAG_OVERFLOW = 2
 EP_FLAG_BAD_ROW = 4
+EP_FLAG_TIMEOUT = 8
 
 LAYOUT_KINDS = {"contiguous": 0, "masked": 1}
 

@@ -9,20 +9,24 @@
 // tokens, one pair per lane (lane l: token l / k of the piece, j = l % k), and
 // give each warp a contiguous run of pieces.  Per piece a warp ranks equal
 // experts with popc(peers & lanemask_lt), the peers coming from one ballot
-// per bit of the expert id, and keeps a running per-warp count of each
-// expert in its own shared-memory row -- no block barrier until every warp
-// has counted.  (match.any gives the peers in one instruction but runs on a
-// shared per-SM unit: 2,048 tokens 6.9 -> 7.8 us.)  Then:
+// per bit of the expert id (ten independent ballots, enough for 1,024
+// experts; the peers of the expert's virtual rank are the same ballots above
+// the rank's shift), and keeps a running per-warp count of each expert in its
+// own shared-memory row -- no block barrier until every warp has counted.
+// (match.any gives the peers in one instruction but runs on a shared per-SM
+// unit: 2,048 tokens 6.9 -> 7.8 us.)  The ids and slots of a lane's pieces
+// live in shared memory: the piece loop is not unrolled (one copy of its code
+// in the instruction cache), and a register array indexed by the loop counter
+// would sit in local memory, whose stores every later warp and cluster
+// barrier waits for.  Then:
 //   single block (layout_block_kernel): one thread per expert turns the warps'
 //     counts into their exclusive prefix over warps and the expert's total;
 //     each warp scans its 32 experts' (padded) totals; after the second
 //     barrier every warp scans the <= 32 range sums with shuffles and each
 //     lane forms its pairs' rows.  Two block barriers in all.
 //   cluster (layout_cluster_kernel, 8 blocks): the same per block, with the
-//     block totals exchanged through distributed shared memory after one
-//     cluster barrier; the blocks then only signal that their remote reads
-//     are done and wait for the others' signals just before exiting, so the
-//     slot assignment overlaps that second cluster barrier.
+//     block totals pushed into every block's shared memory (st.async,
+//     completed on the receiving block's mbarrier) instead of read remotely.
 // The status word is written once, by one thread: bad ids are collected per
 // warp and the masked overflow is read off the expert totals.  The slot of a
 // pair is the number of earlier pairs (flattened t*k + j) with the same
@@ -36,21 +40,19 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-// Pieces per warp a lane keeps (ids and slots): 8 in 1024-thread blocks
-// (64 registers a thread), 16 in smaller ones.
+// Pieces per warp at most (ids and slots in shared memory, ppw * 32 * 8
+// bytes per warp): 8 in 1024-thread blocks, 16 in smaller ones.
 template <int NT>
 __host__ __device__ constexpr int max_pieces() { return NT >= 1024 ? 8 : 16; }
-// The per-piece loops are not unrolled: each pass is the same code, fetched
-// once into the instruction cache (instruction fetch was the top stall of
-// the unrolled form, whose every piece was new code; 128 tokens 4.64 ->
-// 4.30 us); the pieces' ids and slots then live in local memory.
-#ifndef EP_LAYOUT_PIECE_UNROLL
-#define EP_LAYOUT_PIECE_UNROLL 1
+#ifndef EP_LAYOUT_CLUSTER_BLOCKS
+#define EP_LAYOUT_CLUSTER_BLOCKS 8
 #endif
-constexpr int kPieceUnroll = EP_LAYOUT_PIECE_UNROLL;
-constexpr int kClusterBlocks = 8;
+constexpr int kClusterBlocks = EP_LAYOUT_CLUSTER_BLOCKS;
 constexpr int kClusterMaxTokens = 2048;
 constexpr size_t kSmemLimit = 160 * 1024;
+// Bits of an expert id: one ballot each.
+constexpr int kKeyBits = 10;
+static_assert((1 << kKeyBits) >= EP_MAX_EXPERTS, "one ballot per expert-id bit");
 
 // The virtual rank of expert e: e / (E / R), a shift when E / R is a power of two.
 struct RankOf {
@@ -72,10 +74,23 @@ RankOf make_rank_of(int E, int R) {
     return r;
 }
 
-__host__ __device__ __forceinline__ int bits_for(int n) {  // bits that distinguish the ids 0 .. n-1
-    int b = 0;
-    while ((1 << b) < n) ++b;
-    return b > 0 ? b : 1;
+// Peers of this lane: the lanes with valid set whose key has the same bits
+// [lo, kKeyBits) as this lane's (0 for a lane without valid).  m[b] is the
+// ballot of key bit b; keys of valid lanes are below 2^kKeyBits.
+__device__ __forceinline__ unsigned peers_from_bits(unsigned vmask, const unsigned (&m)[kKeyBits],
+                                                    int key, int lo, bool valid) {
+    unsigned p = vmask;
+#pragma unroll
+    for (int b = 0; b < kKeyBits; ++b) {
+        const unsigned sel = ((key >> b) & 1) ? m[b] : ~m[b];
+        p &= b >= lo ? sel : kFullMask;
+    }
+    return valid ? p : 0u;
+}
+
+__device__ __forceinline__ void key_ballots(int key, unsigned (&m)[kKeyBits]) {
+#pragma unroll
+    for (int b = 0; b < kKeyBits; ++b) m[b] = __ballot_sync(kFullMask, (key >> b) & 1);
 }
 
 // Shared-memory arrays of the one-launch layouts (carved by the kernels).
@@ -85,63 +100,82 @@ struct OneLaunchSmem {
     int32_t* off_local;  // [E]  exclusive scan of the padded totals within each 32-expert range
     int32_t* range_sum;  // [32] sum of the padded totals of each 32-expert range
     uint32_t* wflags;    // [NW] condition flags each warp found among its ids
+    int32_t* pe;         // [NW][ppw][32]  expert id of each lane's pair in each piece (-1: none)
+    int32_t* plr;        // [NW][ppw][32]  that pair's slot among its warp's pairs of the expert
     int32_t* btot;       // [E + R_cols + 1]  block totals and the block's flags, read by
                          // the other blocks (cluster)
     int32_t* base;       // [E]  pairs of expert e in the cluster's earlier blocks (cluster)
+    int32_t* ctot;       // [E + R_cols]  cluster totals, stored by block 0 (cluster)
 };
 
-// This lane's pairs: piece q of the warp's run holds pair (t, j) with
-// t = (p0 + q) * P + lane / k, j = lane % k, for lanes below P * k.
-template <int MAXP>
-struct LanePairs {
-    int e[MAXP];   // expert id (-1: no pair, or no expert)
-    int lr[MAXP];  // slot among the warp's pairs with the same expert
-};
+// Zero this warp's rows of expert and rank counts.  Shared memory only, so
+// the kernels do it before waiting for the previous grid.
+__device__ __forceinline__ void zero_warp_rows(const OneLaunchSmem& sm, int E, int R_cols) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int i = lane; i < E; i += 32) sm.cnt[warp * E + i] = 0;
+    for (int i = lane; i < R_cols; i += 32) sm.rc[warp * R_cols + i] = 0;
+    __syncwarp();
+}
 
-// Phase 1 (per warp, no block barrier): load the warp's ids, count them into
-// the warp's row `my_cnt` (and tokens per rank into `my_rc`) and rank each
-// pair among the warp's earlier pairs with the same expert.
+// Phase 1 (per warp, no block barrier): load the warp's ids into my_e, count
+// them into the warp's row `my_cnt` (and tokens per rank into `my_rc`) and
+// store in my_lr each pair's slot among the warp's earlier pairs with the
+// same expert.  my_e / my_lr hold piece q's lane l at [q * 32 + l]; the
+// count rows start zeroed (zero_warp_rows).
 template <bool RANKS, int MAXP>
 __device__ __forceinline__ void warp_count_pieces(const int32_t* __restrict__ idx, int T, int k,
                                                   int E, int R_cols, int P, int p0, int np,
                                                   RankOf rank_of, int32_t* my_cnt,
-                                                  int32_t* my_rc, LanePairs<MAXP>& lp,
+                                                  int32_t* my_rc, int32_t* my_e, int32_t* my_lr,
                                                   uint32_t& flags) {
     const int lane = threadIdx.x & 31;
     const int tl = lane / k;
     const int jl = lane - tl * k;
     const bool used = lane < P * k;
     const unsigned lt = lanemask_lt();
-    const int key_bits = bits_for(E);
-    const int rbits = bits_for(R_cols > 0 ? R_cols : 1);
     // the lanes of this lane's token (for counting each rank once per token)
     const unsigned grp = !used ? 0u : (k >= 32 ? kFullMask : ((1u << k) - 1u) << (tl * k));
+    {
+        int ids[MAXP];  // all loads issued before the first store
 #pragma unroll
-    for (int q = 0; q < MAXP; ++q) {
-        const int t = (p0 + q) * P + tl;
-        lp.e[q] = (q < np && used && t < T) ? __ldg(idx + (int64_t)t * k + jl) : -1;
-        lp.lr[q] = 0;
+        for (int q = 0; q < MAXP; ++q) {
+            const int t = (p0 + q) * P + tl;
+            ids[q] = (q < np && used && t < T) ? __ldg(idx + (int64_t)t * k + jl) : -1;
+        }
+#pragma unroll
+        for (int q = 0; q < MAXP; ++q)
+            if (q < np) my_e[q * 32 + lane] = ids[q];
     }
-    for (int i = lane; i < E; i += 32) my_cnt[i] = 0;
-    if (RANKS)
-        for (int i = lane; i < R_cols; i += 32) my_rc[i] = 0;
-    __syncwarp();
-#pragma unroll kPieceUnroll
-    for (int q = 0; q < MAXP; ++q) {
-        if (q >= np) break;  // warp-uniform
-        const int e = lp.e[q];
+#pragma unroll 1
+    for (int q = 0; q < np; ++q) {  // warp-uniform
+        const int e = my_e[q * 32 + lane];
         const bool valid = e >= 0 && e < E;
         if (e < -1 || e >= E) flags |= EP_FLAG_BAD_EXPERT;
-        const unsigned peers = warp_peers(valid, e, key_bits);
-        if (valid) lp.lr[q] = my_cnt[e] + __popc(peers & lt);
+        unsigned m[kKeyBits];
+        key_ballots(e, m);
+        const unsigned vmask = __ballot_sync(kFullMask, valid);
+        const unsigned peers = peers_from_bits(vmask, m, e, 0, valid);
+        int c = 0;
+        if (valid) {
+            c = my_cnt[e];
+            my_lr[q * 32 + lane] = c + __popc(peers & lt);
+        }
         int r = 0;
         unsigned rpeers = 0;
         if (RANKS) {
             r = valid ? rank_of(e) : 0;
-            rpeers = warp_peers(valid, r, rbits) & grp;  // same token, same rank
+            if (rank_of.shift >= 0) {  // warp-uniform: the rank is the id's upper bits
+                rpeers = peers_from_bits(vmask, m, e, rank_of.shift, valid);
+            } else {
+                unsigned mr[kKeyBits];
+                key_ballots(r, mr);
+                rpeers = peers_from_bits(vmask, mr, r, 0, valid);
+            }
+            rpeers &= grp;  // same token, same rank
         }
         __syncwarp();
-        if (valid && (__ffs(peers) - 1) == lane) my_cnt[e] += __popc(peers);
+        if (valid && (__ffs(peers) - 1) == lane) my_cnt[e] = c + __popc(peers);
         if (RANKS && valid && (rpeers & lt) == 0) atomicAdd(&my_rc[r], 1);  // first of the token
         __syncwarp();
     }
@@ -167,7 +201,7 @@ __device__ __forceinline__ int padded(int c, int align) {
 // become their exclusive prefix over the warps; returns the total.
 template <int NW>
 __device__ __forceinline__ int expert_prefix_over_warps(int32_t* cnt, int E, int e) {
-    constexpr int G = NW < 8 ? NW : 8;  // loads issued together
+    constexpr int G = NW < 16 ? NW : 16;  // loads issued together
     int run = 0;
 #pragma unroll
     for (int w0 = 0; w0 < NW; w0 += G) {
@@ -207,27 +241,26 @@ __device__ __forceinline__ int range_bases(const OneLaunchSmem& sm, int E, int& 
 // earlier blocks (cluster) to the warp's prefix.  Rows go to g_dst (global,
 // if given) and s_dst (shared, if given); a row at or past `rows` raises
 // EP_FLAG_BAD_ROW in `flags`.
-template <int MAXP, typename BaseFn>
-__device__ __forceinline__ void assign_pieces(const LanePairs<MAXP>& lp, int T, int k, int E, int kind,
-                                              int capacity, int P, int p0, int np, int t_end,
-                                              const OneLaunchSmem& sm, const int32_t* my_cnt,
-                                              int rp, int64_t rows, BaseFn base_e,
-                                              int32_t* __restrict__ g_dst, int32_t* s_dst,
-                                              uint32_t& flags) {
+template <typename BaseFn>
+__device__ __forceinline__ void assign_pieces(const int32_t* my_e, const int32_t* my_lr, int k,
+                                              int E, int kind, int capacity, int P, int p0,
+                                              int np, int t_end, const OneLaunchSmem& sm,
+                                              const int32_t* my_cnt, int rp, int64_t rows,
+                                              BaseFn base_e, int32_t* __restrict__ g_dst,
+                                              int32_t* s_dst, uint32_t& flags) {
     const int lane = threadIdx.x & 31;
     const int tl = lane / k;
     const int jl = lane - tl * k;
     const bool used = lane < P * k;
-#pragma unroll kPieceUnroll
-    for (int q = 0; q < MAXP; ++q) {
-        if (q >= np) break;  // warp-uniform
-        const int e = lp.e[q];
+#pragma unroll 1
+    for (int q = 0; q < np; ++q) {  // warp-uniform
+        const int e = my_e[q * 32 + lane];
         const bool valid = e >= 0 && e < E;
         const int rbase = __shfl_sync(kFullMask, rp, valid ? (e >> 5) : 0);
         const int t = (p0 + q) * P + tl;
         int dst = -1;
         if (valid) {
-            const int slot = base_e(e) + my_cnt[e] + lp.lr[q];
+            const int slot = base_e(e) + my_cnt[e] + my_lr[q * 32 + lane];
             if (kind == EP_LAYOUT_CONTIGUOUS) dst = rbase + sm.off_local[e] + slot;
             else if (slot < capacity) dst = e * capacity + slot;  // else overflow: -1
             if ((int64_t)dst >= rows) flags |= EP_FLAG_BAD_ROW;
@@ -238,7 +271,6 @@ __device__ __forceinline__ void assign_pieces(const LanePairs<MAXP>& lp, int T, 
             if (s_dst) s_dst[p] = dst;
         }
     }
-    (void)T;
 }
 
 struct NoBase {
@@ -250,6 +282,7 @@ struct NoBase {
 // the layout's condition flags (bad ids, masked overflow: an expert's count
 // above the capacity), the same in every thread; `row_flags` gets this
 // lane's EP_FLAG_BAD_ROW (a row at or past `rows`).  Two block barriers.
+// The warps' count rows must be zeroed first (zero_warp_rows).
 template <int NT, bool RANKS>
 __device__ __forceinline__ uint32_t block_layout(const int32_t* __restrict__ idx, int T, int k,
                                                  int E, int R_cols, int kind, int capacity,
@@ -268,10 +301,11 @@ __device__ __forceinline__ uint32_t block_layout(const int32_t* __restrict__ idx
     const int p0 = warp * ppw;
     const int np = p0 >= npieces ? 0 : (npieces - p0 < ppw ? npieces - p0 : ppw);
     int32_t* my_cnt = sm.cnt + warp * E;
+    int32_t* my_e = sm.pe + warp * ppw * 32;
+    int32_t* my_lr = sm.plr + warp * ppw * 32;
     uint32_t flags = 0;
-    LanePairs<max_pieces<NT>()> lp;
-    warp_count_pieces<RANKS>(idx, T, k, E, R_cols, P, p0, np, rank_of, my_cnt,
-                             sm.rc + warp * R_cols, lp, flags);
+    warp_count_pieces<RANKS, max_pieces<NT>()>(idx, T, k, E, R_cols, P, p0, np, rank_of, my_cnt,
+                                               sm.rc + warp * R_cols, my_e, my_lr, flags);
     {
         const unsigned wf = __reduce_or_sync(kFullMask, flags);
         if (lane == 0) sm.wflags[warp] = wf;
@@ -313,26 +347,35 @@ __device__ __forceinline__ uint32_t block_layout(const int32_t* __restrict__ idx
         }
         if (threadIdx.x == 0) expert_offsets[E] = total;
     }
-    assign_pieces(lp, T, k, E, kind, capacity, P, p0, np, T, sm, my_cnt, rp, rows, NoBase(),
-                  g_dst, s_dst, row_flags);
+    assign_pieces(my_e, my_lr, k, E, kind, capacity, P, p0, np, T, sm, my_cnt, rp, rows,
+                  NoBase(), g_dst, s_dst, row_flags);
     return lflags;
 }
 
+// Ints of the single-block arrays before the piece state, rounded to 16 bytes.
+__host__ __device__ __forceinline__ int block_head_ints(int NW, int E, int R_cols) {
+    return (NW * (E + R_cols) + E + 32 + NW + 3) & ~3;
+}
+
 // Carve the single-block arrays out of dynamic shared memory.
-__device__ __forceinline__ OneLaunchSmem carve_block(int32_t* p, int NW, int E, int R_cols) {
+__device__ __forceinline__ OneLaunchSmem carve_block(int32_t* p, int NW, int E, int R_cols,
+                                                     int ppw) {
     OneLaunchSmem sm;
     sm.cnt = p;
     sm.rc = sm.cnt + NW * E;
     sm.off_local = sm.rc + NW * R_cols;
     sm.range_sum = sm.off_local + E;
     sm.wflags = reinterpret_cast<uint32_t*>(sm.range_sum + 32);
+    sm.pe = p + block_head_ints(NW, E, R_cols);
+    sm.plr = sm.pe + NW * ppw * 32;
     sm.btot = nullptr;
     sm.base = nullptr;
+    sm.ctot = nullptr;
     return sm;
 }
 
-size_t block_smem_bytes(int NW, int E, int R_cols) {
-    return ((size_t)NW * (E + R_cols + 1) + E + 32) * sizeof(int32_t);
+size_t block_smem_bytes(int NW, int E, int R_cols, int ppw) {
+    return ((size_t)block_head_ints(NW, E, R_cols) + (size_t)2 * NW * ppw * 32) * sizeof(int32_t);
 }
 
 // Small batches: the whole layout in one block.
@@ -344,7 +387,8 @@ layout_block_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
                     int32_t* __restrict__ dst_row, int32_t* __restrict__ rank_token_counts,
                     uint32_t* __restrict__ status) {
     extern __shared__ __align__(16) int32_t smem_i[];
-    const OneLaunchSmem sm = carve_block(smem_i, NT / 32, E, R_cols);
+    const OneLaunchSmem sm = carve_block(smem_i, NT / 32, E, R_cols, ppw);
+    zero_warp_rows(sm, E, R_cols);
     pdl_wait();
     pdl_trigger();
     uint32_t row_flags = 0;  // no row limit here
@@ -355,13 +399,52 @@ layout_block_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     if (threadIdx.x == 0 && status) *status = f;  // the one write of the status word
 }
 
-// Medium batches: ONE launch of one 8-block cluster; block b owns tokens
-// [b * tpb, (b + 1) * tpb).
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// Medium batches: ONE launch of one cluster of kClusterBlocks blocks; block b
+// owns tokens [b * tpb, (b + 1) * tpb).  The blocks exchange their totals by
+// pushing them: each block stores its E + R_cols + 1 totals and flags into
+// slot b of every block's `recv` with st.async, whose bytes complete on the
+// receiving block's mbarrier; a block reads its own recv once its mbarrier
+// has seen all the bytes.  So there is one cluster barrier, arrived at right
+// after the mbarriers are initialised and waited on just before the first
+// push (by then every block has long arrived), and no block reads another's
+// shared memory, so none has to wait for the others before exiting.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void cluster_wait_acquire() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void push_v4(uint32_t remote, const int4& v, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+        ::"r"(remote), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for phase 0 of the mbarrier at `bar` to complete; false if it has not
+// after kPushWaitNs (and at least 2^16 polls, so a context switch alone
+// cannot end the wait).
+constexpr uint64_t kPushWaitNs = 1000000000ull;
+__device__ __forceinline__ bool wait_phase0(uint32_t bar) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t polls = 0;; ++polls) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar)
+            : "memory");
+        if (done) return true;
+        if (polls >= (1u << 16) && global_ns() - t0 > kPushWaitNs) return false;
+    }
 }
 
 template <int NT, bool RANKS>
@@ -373,11 +456,14 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
                       uint32_t* __restrict__ status) {
     constexpr int NW = NT / 32;
     extern __shared__ __align__(16) int32_t smem_i[];
+    __shared__ __align__(8) uint64_t s_bar;
     cg::cluster_group cluster = cg::this_cluster();
     const int b = (int)cluster.block_rank();
-    OneLaunchSmem sm = carve_block(smem_i, NW, E, R_cols);
-    sm.btot = reinterpret_cast<int32_t*>(sm.wflags + NW);  // [E + R_cols + 1]
-    sm.base = sm.btot + E + R_cols + 1;                     // [E]
+    const int nb = (E + R_cols + 1 + 3) & ~3;  // pushed ints per block (16-byte multiple)
+    OneLaunchSmem sm = carve_block(smem_i, NW, E, R_cols, ppw);
+    sm.btot = sm.plr + NW * ppw * 32;             // [nb]  this block's totals, then its flags
+    int32_t* recv = sm.btot + nb;                 // [kClusterBlocks][nb]  every block's btot
+    sm.base = recv + kClusterBlocks * nb;         // [E]
     const int warp = threadIdx.x >> 5;
     const int t0 = b * tpb;
     const int tb = T - t0 < 0 ? 0 : (T - t0 < tpb ? T - t0 : tpb);  // this block's tokens
@@ -385,20 +471,28 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
     const int p0 = warp * ppw;
     const int np = p0 >= npieces ? 0 : (npieces - p0 < ppw ? npieces - p0 : ppw);
     const int32_t* bidx = idx + (int64_t)t0 * k;
+    const uint32_t bar = smem_addr(&s_bar);
+    zero_warp_rows(sm, E, R_cols);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
     pdl_wait();
     pdl_trigger();
     int32_t* my_cnt = sm.cnt + warp * E;
+    int32_t* my_e = sm.pe + warp * ppw * 32;
+    int32_t* my_lr = sm.plr + warp * ppw * 32;
     uint32_t flags = 0;
-    LanePairs<max_pieces<NT>()> lp;
-    warp_count_pieces<RANKS>(bidx, tb, k, E, R_cols, P, p0, np, rank_of, my_cnt,
-                             sm.rc + warp * R_cols, lp, flags);
+    warp_count_pieces<RANKS, max_pieces<NT>()>(bidx, tb, k, E, R_cols, P, p0, np, rank_of,
+                                               my_cnt, sm.rc + warp * R_cols, my_e, my_lr, flags);
     {
         const unsigned wf = __reduce_or_sync(kFullMask, flags);
         if ((threadIdx.x & 31) == 0) sm.wflags[warp] = wf;
     }
     __syncthreads();
-    // block totals (prefix over this block's warps kept in cnt)
+    // block totals (prefix over this block's warps kept in cnt), rank totals, flags
     for (int e = threadIdx.x; e < E; e += NT) sm.btot[e] = expert_prefix_over_warps<NW>(sm.cnt, E, e);
     if (RANKS)
         for (int r = threadIdx.x; r < R_cols; r += NT) {
@@ -407,28 +501,45 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
             for (int w = 0; w < NW; ++w) s += sm.rc[w * R_cols + r];
             sm.btot[E + r] = s;
         }
-    if (threadIdx.x == 0) {  // the block's flags, for block 0
+    if (threadIdx.x == 0) {
         uint32_t bf = 0;
         for (int w = 0; w < NW; ++w) bf |= sm.wflags[w];
         sm.btot[E + R_cols] = (int32_t)bf;
     }
-    cluster.sync();  // every block's totals are complete and visible
-    // one thread per expert: pairs in earlier blocks and the cluster total,
-    // read from the 8 blocks' shared memory; masked overflow is a total above
-    // the capacity
+    for (int i = E + R_cols + 1 + (int)threadIdx.x; i < nb; i += NT) sm.btot[i] = 0;
+    __syncthreads();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every mbarrier is initialised
+    if (threadIdx.x == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(kClusterBlocks * nb * 4))
+                     : "memory");
+    {
+        const uint32_t slot = smem_addr(recv + b * nb);
+        for (int i = threadIdx.x; i < nb / 4; i += NT) {
+            const int4 v = reinterpret_cast<const int4*>(sm.btot)[i];
+#pragma unroll
+            for (int q = 0; q < kClusterBlocks; ++q)
+                push_v4(cluster_map(slot + 16u * i, q), v, cluster_map(bar, q));
+        }
+    }
+    uint32_t cflags = 0;
+    if (!__syncthreads_and(wait_phase0(bar))) {  // a block's totals never arrived: give up
+        if (threadIdx.x == 0 && status) atomicOr(status, EP_FLAG_TIMEOUT);
+        return;
+    }
+    // one thread per expert: pairs in earlier blocks and the cluster total;
+    // masked overflow is a total above the capacity
     int ovf = 0;
     for (int e0 = 0; e0 < E; e0 += NT) {  // block-uniform
         const int e = e0 + threadIdx.x;
         int tt = 0;
         if (e < E) {
-            int v[kClusterBlocks];
-#pragma unroll
-            for (int q = 0; q < kClusterBlocks; ++q) v[q] = cluster.map_shared_rank(sm.btot, q)[e];
             int before = 0, total = 0;
 #pragma unroll
             for (int q = 0; q < kClusterBlocks; ++q) {
-                before += q < b ? v[q] : 0;
-                total += v[q];
+                const int v = recv[q * nb + e];
+                before += q < b ? v : 0;
+                total += v;
             }
             sm.base[e] = before;
             if (b == 0) expert_counts[e] = total;
@@ -442,15 +553,12 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
         for (int r = (int)threadIdx.x - first; r >= 0 && r < R_cols; r += NT) {
             int s = 0;
 #pragma unroll
-            for (int q = 0; q < kClusterBlocks; ++q) s += cluster.map_shared_rank(sm.btot, q)[E + r];
+            for (int q = 0; q < kClusterBlocks; ++q) s += recv[q * nb + E + r];
             rank_token_counts[r] = s;
         }
     }
-    uint32_t cflags = 0;  // block 0: every block's flags
     if (b == 0 && threadIdx.x == 0)
-        for (int q = 0; q < kClusterBlocks; ++q)
-            cflags |= (uint32_t)cluster.map_shared_rank(sm.btot, q)[E + R_cols];
-    cluster_arrive_release();  // this block's remote reads are done
+        for (int q = 0; q < kClusterBlocks; ++q) cflags |= (uint32_t)recv[q * nb + E + R_cols];
     if (__syncthreads_or(ovf)) cflags |= EP_FLAG_OVERFLOW;
     int rp;
     const int total = range_bases(sm, E, rp);
@@ -464,15 +572,16 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
     }
     const int32_t* base = sm.base;
     uint32_t row_flags = 0;  // no row limit here
-    assign_pieces(lp, tb, k, E, kind, capacity, P, p0, np, tb, sm, my_cnt, rp, (int64_t)1 << 40,
-                  [base](int e) { return base[e]; }, dst_row + (int64_t)t0 * k, nullptr,
-                  row_flags);
+    assign_pieces(my_e, my_lr, k, E, kind, capacity, P, p0, np, tb, sm, my_cnt, rp,
+                  (int64_t)1 << 40, [base](int e) { return base[e]; }, dst_row + (int64_t)t0 * k,
+                  nullptr, row_flags);
     if (b == 0 && threadIdx.x == 0 && status) *status = cflags;  // the one write of the status word
-    cluster_wait_acquire();  // no block leaves while another may still read its totals
 }
 
-size_t cluster_smem_bytes(int NW, int E, int R_cols) {
-    return block_smem_bytes(NW, E, R_cols) + ((size_t)2 * E + R_cols + 1) * sizeof(int32_t);
+size_t cluster_smem_bytes(int NW, int E, int R_cols, int ppw) {
+    const size_t nb = (size_t)((E + R_cols + 1 + 3) & ~3);
+    return block_smem_bytes(NW, E, R_cols, ppw) +
+           ((1 + kClusterBlocks) * nb + (size_t)E) * sizeof(int32_t);
 }
 
 // Pieces per warp for `tokens` tokens over NW warps (pieces of P = 32/k tokens).
@@ -554,10 +663,11 @@ layout_dispatch_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int
     extern __shared__ __align__(16) int32_t smem_i[];
     __shared__ uint32_t s_flags;
     int32_t* s_dst = smem_i;  // [T * k] rows of all pairs
-    const OneLaunchSmem sm = carve_block(s_dst + ((T * k + 3) & ~3), NW, E, R_cols);
+    const OneLaunchSmem sm = carve_block(s_dst + ((T * k + 3) & ~3), NW, E, R_cols, ppw);
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const bool lead = blockIdx.x == 0;
+    zero_warp_rows(sm, E, R_cols);
 
     pdl_wait();
     pdl_trigger();
@@ -664,8 +774,9 @@ layout_dispatch_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int
     }
 }
 
-size_t layout_dispatch_smem_bytes(int T, int k, int E, int R_cols) {
-    return ((size_t)((T * k + 3) & ~3)) * sizeof(int32_t) + block_smem_bytes(kLDWarps, E, R_cols);
+size_t layout_dispatch_smem_bytes(int T, int k, int E, int R_cols, int ppw) {
+    return ((size_t)((T * k + 3) & ~3)) * sizeof(int32_t) +
+           block_smem_bytes(kLDWarps, E, R_cols, ppw);
 }
 
 template <bool FP8, bool RANKS>
@@ -695,7 +806,7 @@ cudaError_t launch_layout_dispatch(const int32_t* topk_idx, int64_t T, int k, in
     if (T < 1 || T > kLDMaxTokens) return cudaErrorNotSupported;
     const int R_cols = rank_token_counts ? R : 0;
     const int ppw = pieces_per_warp(T, k, kLDWarps);
-    const size_t smem = layout_dispatch_smem_bytes((int)T, k, E, R_cols);
+    const size_t smem = layout_dispatch_smem_bytes((int)T, k, E, R_cols, ppw);
     if (ppw > max_pieces<kLDThreads>() || smem > kSmemLimit) return cudaErrorNotSupported;
     const RankOf rof = make_rank_of(E, R);
     const RowSlices sl = row_slices(T, fp8 ? H / 16 : H / 8);
@@ -720,7 +831,7 @@ cudaError_t launch_layout_block(const int32_t* topk_idx, int64_t T, int k, int E
     for (int nt = max_threads; nt >= 32; nt /= 2) {
         const int NW = nt / 32;
         const int ppw = pieces_per_warp(T, k, NW);
-        const size_t smem = block_smem_bytes(NW, E, R_cols);
+        const size_t smem = block_smem_bytes(NW, E, R_cols, ppw);
         if (ppw > (nt >= 1024 ? max_pieces<1024>() : max_pieces<512>()) || smem > kSmemLimit)
             continue;
 #define EP_BLOCK_CASE(N)                                                                         \
@@ -759,7 +870,7 @@ cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int
     for (int nt = max_threads; nt >= 32; nt /= 2) {
         const int NW = nt / 32;
         const int ppw = pieces_per_warp(tpb, k, NW);
-        const size_t smem = cluster_smem_bytes(NW, E, R_cols);
+        const size_t smem = cluster_smem_bytes(NW, E, R_cols, ppw);
         if (ppw > (nt >= 1024 ? max_pieces<1024>() : max_pieces<512>()) || smem > kSmemLimit)
             continue;
 #define EP_CLUSTER_CASE(N)                                                                       \

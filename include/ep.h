@@ -79,7 +79,10 @@ typedef enum {
 enum {
     EP_FLAG_BAD_EXPERT = 1u, /* an expert id outside [-1, E): the pair was skipped */
     EP_FLAG_OVERFLOW = 2u,   /* masked layout: slot >= capacity, the pair was dropped */
-    EP_FLAG_BAD_ROW = 4u     /* dispatch/combine: dst_row outside [-1, rows): skipped */
+    EP_FLAG_BAD_ROW = 4u,    /* dispatch/combine: dst_row outside [-1, rows): skipped */
+    EP_FLAG_TIMEOUT = 8u     /* layout: a block of the one-launch cluster layout waited
+                                over a second for the others' totals and gave up; the
+                                outputs are incomplete (not expected on a working GPU) */
 };
 
 typedef enum { EP_LAYOUT_CONTIGUOUS = 0, EP_LAYOUT_MASKED = 1 } ep_layout_kind_t;
