@@ -371,13 +371,19 @@ cudaError_t launch_layout(const int32_t* topk_idx, int64_t T, int k, int E, int 
         if (err != cudaErrorNotSupported) return err;
     }
     if (T <= EP_LAYOUT_CLUSTER_MAX_TOKENS) {
-        const cudaError_t err =
-            launch_layout_cluster(topk_idx, T, k, E, R_cols, R, kind, capacity, align,
-                                  T <= EP_LAYOUT_CLUSTER_SMALL_MAX_TOKENS
-                                      ? EP_LAYOUT_CLUSTER_THREADS_SMALL
-                                      : EP_LAYOUT_CLUSTER_THREADS,
-                                  expert_counts, expert_offsets,
-                                  dst_row, rank_token_counts, status, stream);
+        cudaError_t err = cudaErrorNotSupported;
+        if (T >= EP_LAYOUT_CLUSTER16_MIN_TOKENS)
+            err = launch_layout_cluster(topk_idx, T, k, E, R_cols, R, kind, capacity, align, 16,
+                                        EP_LAYOUT_CLUSTER16_THREADS, expert_counts,
+                                        expert_offsets, dst_row, rank_token_counts, status,
+                                        stream);
+        if (err != cudaErrorNotSupported) return err;
+        err = launch_layout_cluster(topk_idx, T, k, E, R_cols, R, kind, capacity, align, 8,
+                                    T <= EP_LAYOUT_CLUSTER_SMALL_MAX_TOKENS
+                                        ? EP_LAYOUT_CLUSTER_THREADS_SMALL
+                                        : EP_LAYOUT_CLUSTER_THREADS,
+                                    expert_counts, expert_offsets, dst_row, rank_token_counts,
+                                    status, stream);
         if (err != cudaErrorNotSupported) return err;
     }
     const int64_t nchunk = layout_num_chunks(T);

@@ -44,10 +44,6 @@ namespace cg = cooperative_groups;
 // bytes per warp): 8 in 1024-thread blocks, 16 in smaller ones.
 template <int NT>
 __host__ __device__ constexpr int max_pieces() { return NT >= 1024 ? 8 : 16; }
-#ifndef EP_LAYOUT_CLUSTER_BLOCKS
-#define EP_LAYOUT_CLUSTER_BLOCKS 8
-#endif
-constexpr int kClusterBlocks = EP_LAYOUT_CLUSTER_BLOCKS;
 constexpr int kClusterMaxTokens = 2048;
 constexpr size_t kSmemLimit = 160 * 1024;
 // Bits of an expert id: one ballot each.
@@ -399,7 +395,8 @@ layout_block_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_
     if (threadIdx.x == 0 && status) *status = f;  // the one write of the status word
 }
 
-// Medium batches: ONE launch of one cluster of kClusterBlocks blocks; block b
+// Medium batches: ONE launch of one cluster of CB blocks (8, or 16 where the
+// GPU can place a cluster that large); block b
 // owns tokens [b * tpb, (b + 1) * tpb).  The blocks exchange their totals by
 // pushing them: each block stores its E + R_cols + 1 totals and flags into
 // slot b of every block's `recv` with st.async, whose bytes complete on the
@@ -447,7 +444,7 @@ __device__ __forceinline__ bool wait_phase0(uint32_t bar) {
     }
 }
 
-template <int NT, bool RANKS>
+template <int NT, bool RANKS, int CB>
 __global__ void __launch_bounds__(NT)
 layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int R_cols, int kind,
                       int capacity, int align, int P, int ppw, int tpb, RankOf rank_of,
@@ -462,8 +459,8 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
     const int nb = (E + R_cols + 1 + 3) & ~3;  // pushed ints per block (16-byte multiple)
     OneLaunchSmem sm = carve_block(smem_i, NW, E, R_cols, ppw);
     sm.btot = sm.plr + NW * ppw * 32;             // [nb]  this block's totals, then its flags
-    int32_t* recv = sm.btot + nb;                 // [kClusterBlocks][nb]  every block's btot
-    sm.base = recv + kClusterBlocks * nb;         // [E]
+    int32_t* recv = sm.btot + nb;                 // [CB][nb]  every block's btot
+    sm.base = recv + CB * nb;                     // [E]
     const int warp = threadIdx.x >> 5;
     const int t0 = b * tpb;
     const int tb = T - t0 < 0 ? 0 : (T - t0 < tpb ? T - t0 : tpb);  // this block's tokens
@@ -511,14 +508,14 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every mbarrier is initialised
     if (threadIdx.x == 0)
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"((uint32_t)(kClusterBlocks * nb * 4))
+                     "r"((uint32_t)(CB * nb * 4))
                      : "memory");
     {
         const uint32_t slot = smem_addr(recv + b * nb);
         for (int i = threadIdx.x; i < nb / 4; i += NT) {
             const int4 v = reinterpret_cast<const int4*>(sm.btot)[i];
 #pragma unroll
-            for (int q = 0; q < kClusterBlocks; ++q)
+            for (int q = 0; q < CB; ++q)
                 push_v4(cluster_map(slot + 16u * i, q), v, cluster_map(bar, q));
         }
     }
@@ -536,7 +533,7 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
         if (e < E) {
             int before = 0, total = 0;
 #pragma unroll
-            for (int q = 0; q < kClusterBlocks; ++q) {
+            for (int q = 0; q < CB; ++q) {
                 const int v = recv[q * nb + e];
                 before += q < b ? v : 0;
                 total += v;
@@ -553,12 +550,12 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
         for (int r = (int)threadIdx.x - first; r >= 0 && r < R_cols; r += NT) {
             int s = 0;
 #pragma unroll
-            for (int q = 0; q < kClusterBlocks; ++q) s += recv[q * nb + E + r];
+            for (int q = 0; q < CB; ++q) s += recv[q * nb + E + r];
             rank_token_counts[r] = s;
         }
     }
     if (b == 0 && threadIdx.x == 0)
-        for (int q = 0; q < kClusterBlocks; ++q) cflags |= (uint32_t)recv[q * nb + E + R_cols];
+        for (int q = 0; q < CB; ++q) cflags |= (uint32_t)recv[q * nb + E + R_cols];
     if (__syncthreads_or(ovf)) cflags |= EP_FLAG_OVERFLOW;
     int rp;
     const int total = range_bases(sm, E, rp);
@@ -578,10 +575,9 @@ layout_cluster_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int 
     if (b == 0 && threadIdx.x == 0 && status) *status = cflags;  // the one write of the status word
 }
 
-size_t cluster_smem_bytes(int NW, int E, int R_cols, int ppw) {
+size_t cluster_smem_bytes(int NW, int E, int R_cols, int ppw, int CB) {
     const size_t nb = (size_t)((E + R_cols + 1 + 3) & ~3);
-    return block_smem_bytes(NW, E, R_cols, ppw) +
-           ((1 + kClusterBlocks) * nb + (size_t)E) * sizeof(int32_t);
+    return block_smem_bytes(NW, E, R_cols, ppw) + ((1 + CB) * nb + (size_t)E) * sizeof(int32_t);
 }
 
 // Pieces per warp for `tokens` tokens over NW warps (pieces of P = 32/k tokens).
@@ -609,29 +605,49 @@ cudaError_t launch_block_nt(const int32_t* idx, int T, int k, int E, int R_cols,
                       dst_row, rtc, status);
 }
 
-template <int NT, bool RANKS>
+template <int NT, bool RANKS, int CB>
 cudaError_t launch_cluster_nt(const int32_t* idx, int T, int k, int E, int R_cols, int kind,
                               int capacity, int align, int ppw, int tpb, RankOf rof,
                               int32_t* counts, int32_t* offsets, int32_t* dst_row, int32_t* rtc,
                               uint32_t* status, size_t smem, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};
-    auto kern = layout_cluster_kernel<NT, RANKS>;
+    auto kern = layout_cluster_kernel<NT, RANKS, CB>;
     cudaError_t err = prepare(kern, smem, configured);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kClusterBlocks);
+    cfg.gridDim = dim3(CB);
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterBlocks;
+    attr[0].val.clusterDim.x = CB;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    if (CB > 8) {  // above the portable cluster size: allowed per kernel, and only if the
+                   // device can place such a cluster (checked once per device)
+        static std::atomic<uint64_t> allowed{0}, refused{0};
+        int dev = 0;
+        err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        const uint64_t bit = 1ull << (dev & 63);
+        if (refused.load(std::memory_order_acquire) & bit) return cudaErrorNotSupported;
+        if (!(allowed.load(std::memory_order_acquire) & bit)) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            int n = 0;
+            if (err == cudaSuccess) err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (err != cudaSuccess || n < 1) {
+                (void)cudaGetLastError();  // a refused size is not this call's failure
+                refused.fetch_or(bit, std::memory_order_acq_rel);
+                return cudaErrorNotSupported;
+            }
+            allowed.fetch_or(bit, std::memory_order_acq_rel);
+        }
+    }
     return cudaLaunchKernelEx(&cfg, kern, idx, T, k, E, R_cols, kind, capacity, align, 32 / k, ppw,
                               tpb, rof, counts, offsets, dst_row, rtc, status);
 }
@@ -859,31 +875,32 @@ cudaError_t launch_layout_block(const int32_t* topk_idx, int64_t T, int k, int E
     return cudaErrorNotSupported;
 }
 
-cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols,
-                                  int R, int kind, int capacity, int align, int max_threads,
-                                  int32_t* expert_counts, int32_t* expert_offsets,
-                                  int32_t* dst_row, int32_t* rank_token_counts, uint32_t* status,
-                                  cudaStream_t stream) {
-    if (T < 1 || T > kClusterMaxTokens) return cudaErrorNotSupported;
+namespace {
+
+template <int CB>
+cudaError_t launch_cluster_cb(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols, int R,
+                              int kind, int capacity, int align, int max_threads,
+                              int32_t* expert_counts, int32_t* expert_offsets, int32_t* dst_row,
+                              int32_t* rank_token_counts, uint32_t* status, cudaStream_t stream) {
     const RankOf rof = make_rank_of(E, R);
-    const int tpb = (int)((T + kClusterBlocks - 1) / kClusterBlocks);
+    const int tpb = (int)((T + CB - 1) / CB);
     for (int nt = max_threads; nt >= 32; nt /= 2) {
         const int NW = nt / 32;
         const int ppw = pieces_per_warp(tpb, k, NW);
-        const size_t smem = cluster_smem_bytes(NW, E, R_cols, ppw);
+        const size_t smem = cluster_smem_bytes(NW, E, R_cols, ppw, CB);
         if (ppw > (nt >= 1024 ? max_pieces<1024>() : max_pieces<512>()) || smem > kSmemLimit)
             continue;
 #define EP_CLUSTER_CASE(N)                                                                       \
     case N:                                                                                      \
         return R_cols > 0                                                                        \
-                   ? launch_cluster_nt<N, true>(topk_idx, (int)T, k, E, R_cols, kind, capacity,  \
-                                                align, ppw, tpb, rof, expert_counts,      \
-                                                expert_offsets, dst_row, rank_token_counts,      \
-                                                status, smem, stream)                            \
-                   : launch_cluster_nt<N, false>(topk_idx, (int)T, k, E, R_cols, kind,           \
-                                                 capacity, align, ppw, tpb, rof,          \
-                                                 expert_counts, expert_offsets, dst_row,         \
-                                                 rank_token_counts, status, smem, stream);
+                   ? launch_cluster_nt<N, true, CB>(topk_idx, (int)T, k, E, R_cols, kind,        \
+                                                    capacity, align, ppw, tpb, rof,              \
+                                                    expert_counts, expert_offsets, dst_row,      \
+                                                    rank_token_counts, status, smem, stream)     \
+                   : launch_cluster_nt<N, false, CB>(topk_idx, (int)T, k, E, R_cols, kind,       \
+                                                     capacity, align, ppw, tpb, rof,             \
+                                                     expert_counts, expert_offsets, dst_row,     \
+                                                     rank_token_counts, status, smem, stream);
         switch (nt) {
             EP_CLUSTER_CASE(1024)
             EP_CLUSTER_CASE(512)
@@ -895,6 +912,26 @@ cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int
         }
 #undef EP_CLUSTER_CASE
     }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_layout_cluster(const int32_t* topk_idx, int64_t T, int k, int E, int R_cols,
+                                  int R, int kind, int capacity, int align, int cluster_blocks,
+                                  int max_threads, int32_t* expert_counts,
+                                  int32_t* expert_offsets, int32_t* dst_row,
+                                  int32_t* rank_token_counts, uint32_t* status,
+                                  cudaStream_t stream) {
+    if (T < 1 || T > kClusterMaxTokens) return cudaErrorNotSupported;
+    if (cluster_blocks == 16)
+        return launch_cluster_cb<16>(topk_idx, T, k, E, R_cols, R, kind, capacity, align,
+                                     max_threads, expert_counts, expert_offsets, dst_row,
+                                     rank_token_counts, status, stream);
+    if (cluster_blocks == 8)
+        return launch_cluster_cb<8>(topk_idx, T, k, E, R_cols, R, kind, capacity, align,
+                                    max_threads, expert_counts, expert_offsets, dst_row,
+                                    rank_token_counts, status, stream);
     return cudaErrorNotSupported;
 }
 
