@@ -31,6 +31,7 @@
 // expert alignment m > 1 (contiguous only) each expert's segment is padded to
 // a multiple of m rows: the offsets scan ceil(count / m) * m instead.
 #include "ep_internal.cuh"
+#include "ep_layout_onelaunch.cuh"
 
 namespace ep {
 namespace {

@@ -34,6 +34,7 @@
 #include <cooperative_groups.h>
 
 #include "ep_internal.cuh"
+#include "ep_layout_onelaunch.cuh"
 
 namespace ep {
 namespace {
