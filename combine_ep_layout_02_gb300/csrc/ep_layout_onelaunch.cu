@@ -9,9 +9,9 @@
 // tokens, one pair per lane (lane l: token l / k of the piece, j = l % k), and
 // give each warp a contiguous run of pieces.  Per piece a warp ranks equal
 // experts with popc(peers & lanemask_lt), the peers coming from one ballot
-// per bit of the expert id (ten independent ballots, enough for 1,024
-// experts; the peers of the expert's virtual rank are the same ballots above
-// the rank's shift), and keeps a running per-warp count of each expert in its
+// per bit of the expert id (independent ballots: eight up to 256 experts, ten
+// up to 1,024; the peers of the expert's virtual rank are the same ballots
+// above the rank's shift), and keeps a running per-warp count of each expert in its
 // own shared-memory row -- no block barrier until every warp has counted.
 // (match.any gives the peers in one instruction but runs on a shared per-SM
 // unit: 2,048 tokens 6.9 -> 7.8 us.)  The ids and slots of a lane's pieces
@@ -72,22 +72,24 @@ RankOf make_rank_of(int E, int R) {
 }
 
 // Peers of this lane: the lanes with valid set whose key has the same bits
-// [lo, kKeyBits) as this lane's (0 for a lane without valid).  m[b] is the
-// ballot of key bit b; keys of valid lanes are below 2^kKeyBits.
-__device__ __forceinline__ unsigned peers_from_bits(unsigned vmask, const unsigned (&m)[kKeyBits],
+// [lo, B) as this lane's (0 for a lane without valid).  m[b] is the ballot of
+// key bit b; keys of valid lanes are below 2^B.
+template <int B>
+__device__ __forceinline__ unsigned peers_from_bits(unsigned vmask, const unsigned (&m)[B],
                                                     int key, int lo, bool valid) {
     unsigned p = vmask;
 #pragma unroll
-    for (int b = 0; b < kKeyBits; ++b) {
+    for (int b = 0; b < B; ++b) {
         const unsigned sel = ((key >> b) & 1) ? m[b] : ~m[b];
         p &= b >= lo ? sel : kFullMask;
     }
     return valid ? p : 0u;
 }
 
-__device__ __forceinline__ void key_ballots(int key, unsigned (&m)[kKeyBits]) {
+template <int B>
+__device__ __forceinline__ void key_ballots(int key, unsigned (&m)[B]) {
 #pragma unroll
-    for (int b = 0; b < kKeyBits; ++b) m[b] = __ballot_sync(kFullMask, (key >> b) & 1);
+    for (int b = 0; b < B; ++b) m[b] = __ballot_sync(kFullMask, (key >> b) & 1);
 }
 
 // Shared-memory arrays of the one-launch layouts (carved by the kernels).
@@ -113,6 +115,46 @@ __device__ __forceinline__ void zero_warp_rows(const OneLaunchSmem& sm, int E, i
     for (int i = lane; i < E; i += 32) sm.cnt[warp * E + i] = 0;
     for (int i = lane; i < R_cols; i += 32) sm.rc[warp * R_cols + i] = 0;
     __syncwarp();
+}
+
+// The piece loop of phase 1 for ids below 2^B (B ballots per piece).
+template <bool RANKS, int B>
+__device__ __forceinline__ void count_pieces(const int32_t* my_e, int np, int E, RankOf rank_of,
+                                             unsigned grp, unsigned lt, int32_t* my_cnt,
+                                             int32_t* my_rc, int32_t* my_lr, uint32_t& flags) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int q = 0; q < np; ++q) {  // warp-uniform
+        const int e = my_e[q * 32 + lane];
+        const bool valid = e >= 0 && e < E;
+        if (e < -1 || e >= E) flags |= EP_FLAG_BAD_EXPERT;
+        unsigned m[B];
+        key_ballots<B>(e, m);
+        const unsigned vmask = __ballot_sync(kFullMask, valid);
+        const unsigned peers = peers_from_bits<B>(vmask, m, e, 0, valid);
+        int c = 0;
+        if (valid) {
+            c = my_cnt[e];
+            my_lr[q * 32 + lane] = c + __popc(peers & lt);
+        }
+        int r = 0;
+        unsigned rpeers = 0;
+        if (RANKS) {
+            r = valid ? rank_of(e) : 0;
+            if (rank_of.shift >= 0) {  // warp-uniform: the rank is the id's upper bits
+                rpeers = peers_from_bits<B>(vmask, m, e, rank_of.shift, valid);
+            } else {
+                unsigned mr[B];
+                key_ballots<B>(r, mr);
+                rpeers = peers_from_bits<B>(vmask, mr, r, 0, valid);
+            }
+            rpeers &= grp;  // same token, same rank
+        }
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) my_cnt[e] = c + __popc(peers);
+        if (RANKS && valid && (rpeers & lt) == 0) atomicAdd(&my_rc[r], 1);  // first of the token
+        __syncwarp();
+    }
 }
 
 // Phase 1 (per warp, no block barrier): load the warp's ids into my_e, count
@@ -144,38 +186,10 @@ __device__ __forceinline__ void warp_count_pieces(const int32_t* __restrict__ id
         for (int q = 0; q < MAXP; ++q)
             if (q < np) my_e[q * 32 + lane] = ids[q];
     }
-#pragma unroll 1
-    for (int q = 0; q < np; ++q) {  // warp-uniform
-        const int e = my_e[q * 32 + lane];
-        const bool valid = e >= 0 && e < E;
-        if (e < -1 || e >= E) flags |= EP_FLAG_BAD_EXPERT;
-        unsigned m[kKeyBits];
-        key_ballots(e, m);
-        const unsigned vmask = __ballot_sync(kFullMask, valid);
-        const unsigned peers = peers_from_bits(vmask, m, e, 0, valid);
-        int c = 0;
-        if (valid) {
-            c = my_cnt[e];
-            my_lr[q * 32 + lane] = c + __popc(peers & lt);
-        }
-        int r = 0;
-        unsigned rpeers = 0;
-        if (RANKS) {
-            r = valid ? rank_of(e) : 0;
-            if (rank_of.shift >= 0) {  // warp-uniform: the rank is the id's upper bits
-                rpeers = peers_from_bits(vmask, m, e, rank_of.shift, valid);
-            } else {
-                unsigned mr[kKeyBits];
-                key_ballots(r, mr);
-                rpeers = peers_from_bits(vmask, mr, r, 0, valid);
-            }
-            rpeers &= grp;  // same token, same rank
-        }
-        __syncwarp();
-        if (valid && (__ffs(peers) - 1) == lane) my_cnt[e] = c + __popc(peers);
-        if (RANKS && valid && (rpeers & lt) == 0) atomicAdd(&my_rc[r], 1);  // first of the token
-        __syncwarp();
-    }
+    if (E <= 256)  // warp-uniform: ids of up to 8 bits need 8 ballots, not 10
+        count_pieces<RANKS, 8>(my_e, np, E, rank_of, grp, lt, my_cnt, my_rc, my_lr, flags);
+    else
+        count_pieces<RANKS, kKeyBits>(my_e, np, E, rank_of, grp, lt, my_cnt, my_rc, my_lr, flags);
 }
 
 // Inclusive warp scan.

@@ -46,10 +46,14 @@ LAYOUT_CASES = [
     (1, 1, 1, 1), (1, 8, 256, 16), (31, 2, 3, 3), (33, 8, 128, 4), (511, 8, 256, 16),
     (512, 8, 256, 16), (513, 8, 256, 16), (1500, 8, 128, 4), (1500, 32, 1024, 8),
     (1025, 1, 1024, 1024), (2000, 3, 7, 7), (4096, 8, 256, 32), (777, 16, 64, 2),
-    # one-launch boundaries: single block up to 384 tokens, cluster up to 2048;
-    # pieces of 32 // k tokens (k = 5, 32), E / R not a power of two, E > 32 * ranges
+    # one-launch boundaries: a single block up to 64 tokens, an 8-block cluster
+    # up to 256, a 16-block one up to 2048 (smaller blocks or the chunked path
+    # when shared memory runs out); pieces of 32 // k tokens (k = 5, 6, 32),
+    # E / R not a power of two, E > 32 * ranges
     (384, 32, 1024, 1024), (385, 8, 256, 16), (2048, 8, 256, 16), (2048, 32, 1024, 1024),
     (100, 5, 120, 5), (1999, 7, 600, 24), (2049, 8, 128, 4), (128, 8, 128, 4), (300, 1, 33, 11),
+    (64, 8, 256, 16), (65, 8, 128, 4), (256, 8, 256, 16), (257, 8, 256, 16), (257, 6, 96, 3),
+    (2048, 8, 128, 4), (1000, 6, 256, 16), (2048, 1, 1024, 1024), (1536, 4, 1024, 32),
 ]
 
 
