@@ -41,14 +41,14 @@ int cached_device_attribute(cudaDeviceAttr attr, std::atomic<int> (&cache)[64]) 
     return v > 0 ? v : 0;
 }
 
-RowSlices row_slices(int64_t T, int64_t nvec) {
+RowSlices row_slices(int64_t T, int64_t nvec, int warps_per_sm, int64_t min_slice) {
     // SM count per device, read once (it only shapes grids)
     static std::atomic<int> sm_cache[64];
     int sms = cached_device_attribute(cudaDevAttrMultiProcessorCount, sm_cache);
     if (sms <= 0) sms = 1;
-    const int64_t target = (int64_t)sms * EP_SLICE_WARPS_PER_SM;
+    const int64_t target = (int64_t)sms * warps_per_sm;
     int64_t S = 1;
-    while (T * S < target && (nvec + 2 * S - 1) / (2 * S) >= 32) S *= 2;
+    while (T * S < target && (nvec + 2 * S - 1) / (2 * S) >= min_slice) S *= 2;
     if (S == 1) return RowSlices{1, nvec};
     const int64_t slice = ((nvec + S - 1) / S + 31) / 32 * 32;
     return RowSlices{(int)((nvec + slice - 1) / slice), slice};

@@ -18,6 +18,20 @@
 #ifndef EP_DISPATCH_PERSISTENT
 #define EP_DISPATCH_PERSISTENT 0  // 1: large batches on a grid of one block per SM (slower)
 #endif
+#ifndef EP_DISPATCH_SLICE_WARPS_PER_SM
+// Column slices (see row_slices) down to 64 vectors (1 KB) while the grid has
+// fewer than this many warps per SM, on top of the default rule (down to 32
+// vectors below 8 warps per SM), whichever gives more slices.  Measured at
+// H = 2048 (L2 flushed): 2,048 tokens 16.4 -> 14.5 us (4 slices), 4,096
+// tokens 26.7 -> 24.7 us (2 slices), 2,048 x 7168 45.7 -> 44.1 us; 1,024
+// tokens and below unchanged.  Slices of 32 vectors up to this grid size were
+// slower at 1,024 tokens (11.3 us against 10.5), and 64-vector slices at 128
+// tokens (6.6 us against 6.2).
+#define EP_DISPATCH_SLICE_WARPS_PER_SM 48
+#endif
+#ifndef EP_DISPATCH_MIN_SLICE
+#define EP_DISPATCH_MIN_SLICE 64  // 16-byte vectors
+#endif
 #ifndef EP_DISPATCH_STORE_CS
 #define EP_DISPATCH_STORE_CS 1  // evict-first stores for the dispatched rows (0: default policy)
 #endif
@@ -138,7 +152,12 @@ cudaError_t launch_dispatch_bf16(const void* x, int64_t T, int64_t H, int k,
                                  uint32_t* status, cudaStream_t stream, bool early) {
     if (T == 0) return cudaSuccess;
     const int64_t nvec = H / 8;
-    const RowSlices sl = row_slices(T, nvec);
+    // few tokens: slices down to 32 vectors while the grid is small; more
+    // tokens: slices down to EP_DISPATCH_MIN_SLICE vectors up to a larger grid
+    RowSlices sl = row_slices(T, nvec);
+    const RowSlices wide =
+        row_slices(T, nvec, EP_DISPATCH_SLICE_WARPS_PER_SM, EP_DISPATCH_MIN_SLICE);
+    if (wide.S > sl.S) sl = wide;
     const unsigned grid = (unsigned)((T * sl.S + kDispatchWarps - 1) / kDispatchWarps);
     if (T < EP_DISPATCH_PREFETCH_MIN_TOKENS)
         return launch_pdl(early ? dispatch_bf16_kernel<EP_DISPATCH_U, false, true>

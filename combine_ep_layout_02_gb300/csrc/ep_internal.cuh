@@ -336,9 +336,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // per token leaves most SMs idle when there are few tokens, so each row is
 // then split into S slices of `slice` 16-byte vectors (a multiple of 32: one
 // vector per lane), one warp per (token, slice).  S doubles while the grid is
-// below EP_SLICE_WARPS_PER_SM warps per SM and the slices stay >= 32 vectors;
-// S = 1 (slice = nvec) otherwise.  The choice only shapes the grid: every
-// output element is still computed by exactly one lane, in the same order.
+// below `warps_per_sm` warps per SM and the slices stay >= `min_slice`
+// vectors (a multiple of 32); S = 1 (slice = nvec) otherwise.  The choice
+// only shapes the grid: every output element is still computed by exactly
+// one lane, in the same order.
 #ifndef EP_SLICE_WARPS_PER_SM
 #define EP_SLICE_WARPS_PER_SM 8
 #endif
@@ -346,7 +347,8 @@ struct RowSlices {
     int S;          // slices (warps) per token
     int64_t slice;  // 16-byte vectors per slice
 };
-RowSlices row_slices(int64_t T, int64_t nvec);
+RowSlices row_slices(int64_t T, int64_t nvec, int warps_per_sm = EP_SLICE_WARPS_PER_SM,
+                     int64_t min_slice = 32);
 
 // The host-side argument checks of ep_layout (EP_OK when the call may
 // proceed); `workspace` / `workspace_bytes` are what the layout would use.
