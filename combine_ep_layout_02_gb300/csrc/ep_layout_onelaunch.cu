@@ -24,7 +24,7 @@
 //     each warp scans its 32 experts' (padded) totals; after the second
 //     barrier every warp scans the <= 32 range sums with shuffles and each
 //     lane forms its pairs' rows.  Two block barriers in all.
-//   cluster (layout_cluster_kernel, 8 blocks): the same per block, with the
+//   cluster (layout_cluster_kernel, 8 or 16 blocks): the same per block, with the
 //     block totals pushed into every block's shared memory (st.async,
 //     completed on the receiving block's mbarrier) instead of read remotely.
 // The status word is written once, by one thread: bad ids are collected per

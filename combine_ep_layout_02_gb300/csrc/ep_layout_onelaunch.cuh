@@ -14,9 +14,10 @@ namespace ep {
 // cannot place 16); cudaErrorNotSupported (nothing enqueued) when the shape
 // does not fit their registers or shared memory.  Sizes measured fastest
 // (graph-replayed, E = 128 and 256): one 256-thread block up to 64 tokens
-// (2.8-3.0 us), 8 blocks of 256 threads up to 256 tokens (128: 3.0-3.2 us;
-// 16 blocks 3.1-3.5 us), 16 blocks of 256 threads above (2048: 4.6-5.0 us;
-// 16 x 512 threads the same; 8 x 512 threads 5.8-5.9 us).  The 8-block
+// (2.7-3.0 us), 8 blocks of 256 threads up to 256 tokens (128: 2.9-3.3 us;
+// 16 blocks 3.1-3.5 us; 8 blocks of 128 threads the same or slower), 16
+// blocks of 256 threads above (2048: 4.4-5.1 us; 16 x 512 threads 4.8-5.2 us;
+// 8 x 512 threads 5.8-5.9 us).  The 8-block
 // fallback keeps 256-thread blocks up to EP_LAYOUT_CLUSTER_SMALL_MAX_TOKENS
 // tokens and 512-thread blocks above.
 #ifndef EP_LAYOUT_BLOCK_MAX_TOKENS
