@@ -522,6 +522,9 @@ def test_dispatch_fp8_every_pattern_at_fixed_scales():
     (256, 8, 256, 16, "masked", 256, 1024, False, 0, True),        # bad ids, two launches
     (100, 8, 64, 4, "contiguous", 0, 512, False, 7, False),        # rows too few: BAD_ROW
     (257, 8, 256, 16, "contiguous", 0, 1024, True, 0, False),      # above the fused range
+    (300, 8, 64, 4, "contiguous", 0, 512, True, 7, False),         # two launches, rows too few
+    (1000, 8, 64, 4, "masked", 200, 512, False, 3000, False),      # masked rows past the buffer
+    (129, 6, 96, 3, "masked", 40, 2048, False, 0, True),           # overflow, bad ids, 30-lane pieces
     (3000, 8, 256, 16, "masked", 3000, 512, False, 0, False),
     # two launches, the dispatch reading x before the layout ends: the
     # decode-like FP8 shape, the masked BF16 shape, and the large-batch
