@@ -22,9 +22,9 @@
 //               each warp walks its pairs 32 at a time in flattened order,
 //               ranking equal experts with popc(peers & lanemask_lt), where the
 //               peers of a lane (lanes holding the same expert) come from one
-//               ballot per bit of the expert id -- a handful of vote
-//               instructions instead of match.any, whose per-SM throughput
-//               made it the bottleneck of this kernel.  The
+//               ballot per bit of the expert id (8 or 10 independent votes)
+//               instead of match.any, whose per-SM throughput made it the
+//               bottleneck of this kernel.  The
 //               slot of a pair is the number of earlier pairs with the same
 //               expert: a stable, deterministic assignment.
 // Masked layouts use the same slots with row = e * capacity + slot.  With an
@@ -230,6 +230,20 @@ __device__ void block_exclusive_scan(const int32_t* in, int E, int32_t* s_off, i
     __syncthreads();
 }
 
+// Peers of this lane: the lanes with valid set whose id equals this lane's,
+// from B independent ballots, one per id bit (valid ids are below 2^B).
+template <int B>
+__device__ __forceinline__ unsigned peers_of_id(bool valid, int e) {
+    unsigned p = __ballot_sync(kFullMask, valid);
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+        const unsigned m = __ballot_sync(kFullMask, (e >> b) & 1);
+        p &= ((e >> b) & 1) ? m : ~m;
+    }
+    return valid ? p : 0u;
+}
+static_assert(EP_MAX_EXPERTS <= 1024, "ten id bits");
+
 __global__ void __launch_bounds__(kLayoutThreads)
 layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, int kind,
                      int capacity, int align, int64_t nchunk, const int32_t* __restrict__ ws,
@@ -299,16 +313,17 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     __syncthreads();
 
     const unsigned lt = lanemask_lt();
-    const int key_bits = 32 - __clz(E - 1 > 0 ? E - 1 : 1);  // bits that distinguish ids in [0, E)
     const int64_t npairs = (int64_t)ntok * k;
     int32_t* out = dst_row + t0 * k;
+    uint32_t flags = 0;
     for (int m = 0; m < k; ++m) {
         const int lp = wp0 + m * 32 + lane;   // pair within the chunk
         const bool in_range = lp < npairs;
         const int e = s_idx[lp];
         const bool valid = (e >= 0) && (e < E);
         const bool bad = in_range && !valid && e != -1;
-        const unsigned peers = warp_peers(valid, e, key_bits);
+        // warp-uniform: eight ballots up to 256 experts, ten above
+        const unsigned peers = E <= 256 ? peers_of_id<8>(valid, e) : peers_of_id<10>(valid, e);
         bool overflow = false;
         int dst = -1;
         if (valid) {
@@ -325,9 +340,11 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
         __syncwarp();
         if (valid && (__ffs(peers) - 1) == lane) my_w[e] += __popc(peers);
         __syncwarp();
-        warp_flag(status, bad, EP_FLAG_BAD_EXPERT);
-        warp_flag(status, overflow, EP_FLAG_OVERFLOW);
+        if (bad) flags |= EP_FLAG_BAD_EXPERT;
+        if (overflow) flags |= EP_FLAG_OVERFLOW;
     }
+    const unsigned wf = __reduce_or_sync(kFullMask, flags);  // one atomic per warp at most
+    if (wf && lane == 0 && status) atomicOr(status, wf);
 }
 
 // T == 0: write the (all-zero) outputs so that callers always get defined data.
