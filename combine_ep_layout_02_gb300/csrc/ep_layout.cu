@@ -111,11 +111,12 @@ layout_count_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, in
     const int64_t left = T - t0;
     const int ntok = left < kLayoutTokensPerChunk ? (int)left : kLayoutTokensPerChunk;
 
+    // shared memory only: before waiting for the previous grid
+    for (int i = threadIdx.x; i < ncol; i += blockDim.x) s_hist[i] = 0;
+    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
     pdl_wait();
     pdl_trigger();
     if (c == 0 && threadIdx.x == 0 && status) *status = 0u;
-    for (int i = threadIdx.x; i < ncol; i += blockDim.x) s_hist[i] = 0;
-    if (R_cols > 0) fill_rank_table(E, R_cols, s_rank_of);
     stage_ids(idx, t0 * k, ntok * k, npad, s_idx);
     __syncthreads();
 
@@ -265,6 +266,7 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
     const int64_t left = T - t0;
     const int ntok = left < kLayoutTokensPerChunk ? (int)left : kLayoutTokensPerChunk;
 
+    for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s_w[i] = 0;  // shared only
     pdl_wait();
     pdl_trigger();
     // issue every global load of the prologue before the first shared store
@@ -285,7 +287,6 @@ layout_assign_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, i
             s_base[e] = base_v[q];
         }
     }
-    for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) s_w[i] = 0;
     __syncthreads();
     block_exclusive_scan<kLayoutThreads>(s_tot, E, s_off, s_warp);
     if (c == 0)
