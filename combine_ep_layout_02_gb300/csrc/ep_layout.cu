@@ -2,8 +2,8 @@
 // scan and stable slot assignment (the "dispatch layout" that the Prefill-like
 // profile of awsome-distributed-ai PR #1238 times inside its boundary).
 //
-// Batches of up to 2048 tokens take one launch (a single block or one 8-block
-// cluster, in ep_layout_onelaunch.cu); larger batches use three small
+// Batches of up to 2048 tokens take one launch (a single block or one cluster
+// of 8 or 16 blocks, in ep_layout_onelaunch.cu); larger batches use three small
 // kernels chained with programmatic dependent launch, where no block ever
 // waits on another block:
 //   1. count  : one 128-thread block per chunk of 128 tokens.  The chunk's
