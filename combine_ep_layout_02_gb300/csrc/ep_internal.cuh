@@ -95,18 +95,6 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Lanes of the warp whose (valid) key equals this lane's: one ballot per key
-// bit.  Invalid lanes get an empty set and appear in no valid lane's set.
-__device__ __forceinline__ unsigned warp_peers(bool valid, int key, int key_bits) {
-    unsigned peers = __ballot_sync(kFullMask, valid);
-    for (int b = 0; b < key_bits; ++b) {
-        const bool bit = (key >> b) & 1;
-        const unsigned ones = __ballot_sync(kFullMask, bit);
-        peers &= bit ? ones : ~ones;
-    }
-    return valid ? peers : 0u;
-}
-
 // OR device-side condition bits into the optional status word: one atomic
 // per warp at most.
 __device__ __forceinline__ void warp_flag(uint32_t* status, bool cond, uint32_t bit) {
