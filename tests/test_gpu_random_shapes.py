@@ -1,5 +1,5 @@
 """Randomised shapes through the whole path (layout, BF16 and FP8 dispatch,
-combine) against the oracle, plus the path captured in a CUDA graph on a
+BF16 and FP8 combine) against the oracle, plus the path captured in a CUDA graph on a
 non-default stream and replayed."""
 import numpy as np
 import pytest
@@ -73,6 +73,16 @@ def test_random_shapes_end_to_end(seed):
     assert np.array_equal(_bits(out), oracle.combine_fp32_seq(yb, wb, ref["dst_row"]))
     _, r64, absum = oracle.combine_f64(yb, wb, ref["dst_row"])
     check_combine(_bits(out), r64, absum, "seed %d" % seed)
+    if H % 128 == 0:
+        # FP8 expert outputs: finite e4m3 codes (no 0x7F / 0xFF) and positive block scales
+        codes = torch.randint(0, 254, (max(rows, 1), H), generator=g, device=DEV)
+        codes = torch.where(codes >= 0x7F, codes + 1, codes).to(torch.uint8)
+        scales = torch.rand(max(rows, 1), H // 128, generator=g, device=DEV) * 4 + 2.0 ** -6
+        out8 = ep.combine_fp8(codes, scales, w, lay.dst_row)
+        qh, sh = codes.cpu().numpy(), scales.cpu().numpy()
+        assert np.array_equal(_bits(out8), oracle.combine_fp8_fp32_seq(qh, sh, wb, ref["dst_row"]))
+        _, r64, absum = oracle.combine_fp8_f64(qh, sh, wb, ref["dst_row"])
+        check_combine(_bits(out8), r64, absum, "fp8 seed %d" % seed)
 
 
 def test_whole_path_in_cuda_graph_on_side_stream():
